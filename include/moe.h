@@ -1,0 +1,187 @@
+/*
+ * moe.h - C ABI of the decode-time routed Mixture-of-Experts layer (GB300, sm_103a).
+ *
+ * One context holds one stack of MoE layers: a router per layer, the routed experts
+ * stored in a low-bit format, and an optional always-on shared expert.  For every
+ * token the layer
+ *   1. runs the router GEMV  logit[e] = sum_h x[h] * W_r[e,h]  (fp32),
+ *   2. picks the top-k experts by logit (equal logits: the lower expert id first) and
+ *      weights them, either softmax renormalised over the k selected, or sigmoid
+ *      scores divided by their sum over the k selected,
+ *   3. applies only the selected experts' SwiGLU FFN  y_e = W_d (silu(W_g x) * (W_u x)),
+ *      dequantising their low-bit weights on the fly,
+ *   4. combines  out = sum_j w_j y_{e_j}  in rank order, then adds the shared expert.
+ * Sources: "WISP - streaming what can't run" (molayo1419.me), section "Insight
+ * (Credit: JustVugg / Colibri)": the model's own router picks the experts of each
+ * token, and only those are fetched; section "Lesson 2: the model's router is the
+ * best scheduler".  "Introducing WARP" (discuss.pytorch.kr), section "The paradox in
+ * WARP's cache settings": num_experts_per_token (k) is a parameter of the model.
+ *
+ * Expert weights (boundary blob formats, little-endian, one contiguous record per
+ * expert: "2.78T-parameter model on a laptop: the NVMe streaming inference engine
+ * WASTE" (ttj.ttj.kr), section "Idle weights only need to arrive on time": each
+ * expert record holds gate, up and down adjacent so one read fetches an expert; the
+ * experts are residual-vector-quantised at 3.00 bits per weight and never expanded):
+ *
+ *   MOE_W_RVQ3_G8: for each matrix in the order gate [F,H], up [F,H], down [H,F]
+ *     (rows x K, K = the input dimension):
+ *       fp16 codebooks [3][256][8]  (stage 0, 1, 2),
+ *       uint8 codes    [rows][K/8][3] (stage order 0, 1, 2 within a group),
+ *     and W[r, 8q+i] = C0[c0][i] + C1[c1][i] + C2[c2][i].  K must be a multiple of 8.
+ *   MOE_W_INT4_G128: for each matrix in the same order:
+ *       uint8 nibbles [rows][K/2] (low nibble = even input index; two's complement
+ *       q in [-8, 7]), then fp16 scales [rows][K/128]; W[r,k] = q[r,k] * s[r,k/128].
+ *     K must be a multiple of 128.
+ *
+ * Experts live either all resident in HBM (hbm_cache_bytes == 0) or in a pinned host
+ * pool with a bounded HBM LRU cache filled on a miss over a side stream ("WISP",
+ * sections "Insight" (VRAM -> RAM -> SSD lookup with LRU promotion) and
+ * "Double-Buffer Async Pipeline"; "WASTE", section "Idle weights only need to arrive
+ * on time": the remaining memory is a bounded expert cache).  Caching changes timing,
+ * never results ("Introducing WARP", section "How WARP keeps the model out of RAM").
+ *
+ * Conventions shared by every call:
+ *   - Return MOE_OK or an error; nothing is thrown.  Argument errors are reported at
+ *     once and leave the context unchanged.
+ *   - Asynchronous CUDA failures and device wait time-outs are sticky: once seen, every
+ *     later call on the context returns MOE_ECUDA or MOE_ETIMEOUT until moe_destroy.
+ *   - Host pointers are copied during the call; the caller may free them on return.
+ *   - Device pointers (x, out) belong to the caller and must stay valid until the
+ *     stream has run the call.
+ *   - A context is single-threaded.  All forwards on one context must be ordered on
+ *     the device (one stream, or streams the caller orders), because they share the
+ *     context's scratch buffers.
+ *   - "stream" is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_EINVAL = 1,     /* bad argument (null, out of range, size mismatch) */
+    MOE_ENOMEM = 2,     /* HBM or pinned host memory could not be allocated */
+    MOE_EBUDGET = 3,    /* the HBM cache cannot hold one layer's working set (2 k records) */
+    MOE_ECUDA = 4,      /* a CUDA call failed (sticky) */
+    MOE_ESTATE = 5,     /* a router or expert of the layer is not registered yet */
+    MOE_ETIMEOUT = 6,   /* a bounded device wait ran out (sticky) */
+    MOE_ENOTFOUND = 7   /* nothing recorded yet (moe_get_routing before a forward) */
+} moe_status;
+
+typedef enum {
+    MOE_ROUTER_SOFTMAX_TOPK_RENORM = 0, /* w = softmax of the k selected logits */
+    MOE_ROUTER_SIGMOID_TOPK_NORM = 1    /* w = sigmoid(l_j) / sum_sel sigmoid(l) */
+} moe_router;
+
+typedef enum {
+    MOE_W_RVQ3_G8 = 1,   /* 3 x uint8 codes per 8 weights, 3 fp16 256x8 codebooks per matrix */
+    MOE_W_INT4_G128 = 2  /* symmetric int4, fp16 scale per 128 input elements */
+} moe_wfmt;
+
+typedef struct {
+    int num_layers;     /* >= 1 */
+    int hidden;         /* H */
+    int ffn;            /* F of every routed expert */
+    int num_experts;    /* E routed experts per layer, 1..1024 */
+    int top_k;          /* k, 1..min(E, 32) */
+    int shared_ffn;     /* 0 = no shared expert, else must equal ffn */
+    int router;         /* moe_router */
+    int wfmt;           /* moe_wfmt */
+    int max_tokens;     /* largest T of a forward, 1..256 */
+    unsigned long long hbm_cache_bytes; /* 0 = every expert resident in HBM; else the
+                                           HBM budget of the expert cache in bytes */
+} moe_config;
+
+typedef struct {
+    unsigned long long forwards;              /* moe_forward calls that ran */
+    unsigned long long tokens;                /* sum of T over those calls */
+    unsigned long long lookups;               /* one per (layer, forward, unique expert) */
+    unsigned long long hits;                  /* lookups served from HBM */
+    unsigned long long misses;                /* lookups copied from the host pool */
+    unsigned long long bytes_expert_touched;  /* kernel-layout record bytes of the unique
+                                                 experts of each forward (incl. shared) */
+    unsigned long long bytes_router;          /* router weight bytes read */
+    unsigned long long bytes_h2d;             /* expert bytes copied host -> device */
+    unsigned long long record_bytes;          /* kernel-layout bytes of one expert */
+    unsigned long long cache_slots;           /* HBM expert slots (0 when all resident) */
+    double h2d_ms;                            /* summed wall time of miss copies (streamed) */
+} moe_stats_t;
+
+typedef struct moe_ctx moe_ctx;
+
+/* Create a context on CUDA device `device`.  Allocates the HBM expert storage (all
+ * experts when hbm_cache_bytes == 0, else floor(hbm_cache_bytes / record) slots),
+ * the pinned host pool (streamed mode only), router storage and scratch.
+ * Errors: MOE_EINVAL (bad config), MOE_EBUDGET (cache below 2 k records, or above what
+ * the pool needs is allowed and clipped), MOE_ENOMEM (HBM or host memory short; checked
+ * against cudaMemGetInfo before allocating), MOE_ECUDA. */
+moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out);
+
+/* Register the router of `layer`: fp32 [E][H] row-major.  `w` may be host memory or
+ * device memory of the context's device; it is copied. */
+moe_status moe_register_router(moe_ctx* ctx, int layer, const float* w);
+
+/* Register expert `expert` (0..E-1, or -1 for the shared expert) of `layer` from its
+ * boundary blob (format above).  `blob` may be host memory or device memory of the
+ * context's device; `bytes` must equal moe_expert_blob_bytes().  The blob is repacked
+ * into the kernel layout: into its HBM slot (resident mode) or into the pinned host
+ * pool (streamed mode).  Synchronous: the blob may be freed on return. */
+moe_status moe_register_expert(moe_ctx* ctx, int layer, int expert, const void* blob, size_t bytes);
+
+/* Size in bytes of one expert blob in the boundary format, or 0 for a bad shape. */
+size_t moe_expert_blob_bytes(int wfmt, int hidden, int ffn);
+
+/* One MoE layer on T tokens: out[T,H] (fp32) = combine of the routed experts (+ shared)
+ * applied to x[T,H] (bf16 bits, row-major).  x and out are device pointers.
+ * Resident mode: fully stream-ordered, never blocks the host, capturable in a CUDA
+ * graph.  Streamed mode: blocks the host once per call to read the routing back, then
+ * issues the miss copies on a side stream, hits first, each missed expert's kernels
+ * waiting for its own copy.  Errors: MOE_EINVAL (T outside 1..max_tokens, layer out of
+ * range, null pointers), MOE_ESTATE (layer not fully registered), sticky errors. */
+moe_status moe_forward(moe_ctx* ctx, int layer, const void* x_bf16, float* out, int T, void* stream);
+
+/* The routing of the last forward of `layer`: idx[T][k] (int32, descending score) and
+ * w[T][k] (fp32) into host buffers; *T_out = that forward's T.  Synchronises the device.
+ * MOE_ENOTFOUND before the first forward of the layer. */
+moe_status moe_get_routing(moe_ctx* ctx, int layer, int* idx, float* w, int* T_out);
+
+/* Residual + RMS norm of the stack that feeds one layer into the next:
+ *   if y != NULL: x += y;   xn = bf16(x / sqrt(mean(x^2) + eps))   (no gain),
+ * on T rows of H = the context's hidden size; x fp32 [T,H] in/out, y fp32 [T,H],
+ * xn bf16 bits [T,H], all device pointers, stream-ordered. */
+moe_status moe_residual_rmsnorm(moe_ctx* ctx, float* x, const float* y, uint16_t* xn, int T,
+                                float eps, void* stream);
+
+/* Counters since create (or the last reset).  Also surfaces sticky asynchronous errors
+ * (it synchronises the context's device). */
+moe_status moe_stats(moe_ctx* ctx, moe_stats_t* out);
+moe_status moe_reset_stats(moe_ctx* ctx);
+
+/* Release everything the context owns.  Safe on NULL. */
+moe_status moe_destroy(moe_ctx* ctx);
+
+const char* moe_strerror(moe_status s);
+
+/* ---- test hooks (no counterpart in the pages; failure injection on the host) ---- */
+
+/* Make the next `n` host-to-device miss copies fail as if cudaMemcpyAsync had
+ * returned an error; the forward then fails with the sticky MOE_ECUDA. */
+moe_status moe_debug_fail_copies(moe_ctx* ctx, int n);
+
+/* Run one bounded device wait on a flag that nothing sets, with a budget of `cycles`
+ * SM clock cycles, on `stream`, and report the status word it leaves: MOE_ETIMEOUT is
+ * the expected answer.  The time-out is recorded in *status only; it does not make the
+ * context sticky. */
+moe_status moe_debug_wait_timeout(moe_ctx* ctx, unsigned long long cycles, void* stream, int* status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

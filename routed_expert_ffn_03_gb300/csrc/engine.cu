@@ -1,0 +1,778 @@
+// engine.cu - the C ABI of include/moe.h: context, expert registry, HBM expert cache,
+// forward orchestration.  Host code; every step of the layer runs in this library's
+// kernels (router.cu, int4.cu, rvq.cu, combine.cu, repack.cu).
+//
+// Expert storage ("WISP - streaming what can't run", section "Insight (Credit: JustVugg
+// / Colibri)": VRAM is checked first, then RAM, with LRU promotion; "2.78T-parameter
+// model on a laptop: the NVMe streaming inference engine WASTE", section "Idle weights
+// only need to arrive on time": the rest of memory is a bounded expert cache, one
+// contiguous record per expert):
+//   resident  - every expert's record lives in HBM for the life of the context;
+//   streamed  - records live in a pinned host pool; an HBM cache of fixed-size slots
+//               holds the recently used ones, least recently used evicted first.  The
+//               current layer's experts are pinned while it runs.  Misses are copied
+//               host-to-device on a side stream; the hits' kernels run first and each
+//               missed expert's kernels wait only for its own copy, so a copy overlaps
+//               the compute of the experts before it ("WISP", section "Double-Buffer
+//               Async Pipeline").  The shared expert and the routers stay resident.
+// Caching changes only timing: the kernels compute each expert pass the same way and
+// the combine sums in a fixed order ("Introducing WARP", section "How WARP keeps the
+// model out of RAM": prediction changes timing, never results).
+#include <sys/sysinfo.h>
+#include <unistd.h>
+
+#include <chrono>
+#include <cstdio>
+#include <cstring>
+#include <list>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+cudaError_t int4_set_attributes();
+cudaError_t rvq_set_attributes();
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+constexpr unsigned long long kDefaultBudget = 2000000000ull;  // ~1 s of SM clock
+
+struct DeviceGuard {
+  int old = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&old);
+    if (old != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (old >= 0 && cur != old) cudaSetDevice(old);
+  }
+};
+
+size_t host_available_bytes() {
+  FILE* f = fopen("/proc/meminfo", "r");
+  if (f) {
+    char key[64];
+    unsigned long long v;
+    char unit[16];
+    while (fscanf(f, "%63s %llu %15s", key, &v, unit) == 3) {
+      if (strcmp(key, "MemAvailable:") == 0) {
+        fclose(f);
+        return (size_t)v * 1024ull;
+      }
+    }
+    fclose(f);
+  }
+  struct sysinfo si;
+  if (sysinfo(&si) == 0) return (size_t)si.freeram * si.mem_unit;
+  return 0;
+}
+
+}  // namespace
+
+struct moe_ctx {
+  moe_config cfg{};
+  int device = 0, num_sms = 0, pmax = 1;
+  RecGeom rg{};
+  size_t rec_bytes = 0, blob_bytes = 0;
+  bool streamed = false;
+  int has_shared = 0;
+  int E1 = 0;  // records per layer in the resident slab (E + shared)
+
+  uint8_t* d_slab = nullptr;     // resident: [L][E1] records; streamed: slots
+  size_t n_slots = 0;
+  uint8_t* d_shared = nullptr;   // streamed: [L] shared records
+  uint8_t* h_pool = nullptr;     // streamed: pinned [L][E] records
+  float* d_router = nullptr;     // [L][E][H]
+  std::vector<char> router_ok, expert_ok;
+
+  uint8_t** d_rec_table = nullptr;  // resident: [L][E+1]; streamed: [E+1]
+  uint8_t** h_table = nullptr;      // streamed: pinned [E+1]
+  int* d_order = nullptr;           // streamed: [max_pass]
+  int* h_order = nullptr;           // pinned
+
+  // LRU cache (streamed)
+  std::vector<long long> slot_key;
+  std::unordered_map<long long, int> where;
+  std::list<int> lru;  // front = most recent
+  std::vector<std::list<int>::iterator> lru_it;
+  std::vector<char> slot_in_lru, slot_pinned;
+
+  // scratch
+  float* d_rpart = nullptr;
+  unsigned int* d_ticket = nullptr;
+  PlanPtrs plan{};
+  void* d_plan_mem = nullptr;
+  int* d_store_idx = nullptr;
+  float* d_store_w = nullptr;
+  std::vector<int> last_T;
+  float* d_part_gu = nullptr;
+  float* d_part_d = nullptr;
+  int max_pass = 0;
+  uint32_t* d_status = nullptr;
+  uint32_t* d_dbg_status = nullptr;
+  DevCounters* d_counters = nullptr;
+  int* h_rb = nullptr;  // pinned readback: hdr(4) | uniq[E] | pass_expert[max_pass]
+
+  cudaStream_t side = nullptr, reg = nullptr;
+  std::vector<cudaEvent_t> copy_ev;
+  uint8_t* d_blob_stage = nullptr;
+  uint8_t* d_rec_stage = nullptr;
+
+  unsigned long long hits = 0, misses = 0, bytes_h2d = 0;
+  double h2d_ms = 0.0;
+  int fail_copies = 0;
+  moe_status sticky = MOE_OK;
+  unsigned long long budget = kDefaultBudget;
+};
+
+namespace {
+
+moe_status cuda_fail(moe_ctx* c) {
+  if (c->sticky == MOE_OK) c->sticky = MOE_ECUDA;
+  return c->sticky;
+}
+
+#define CK(call)                          \
+  do {                                    \
+    cudaError_t e_ = (call);              \
+    if (e_ != cudaSuccess) return cuda_fail(c); \
+  } while (0)
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// Map the device status word to a sticky status (synchronises the device).
+moe_status check_device(moe_ctx* c) {
+  if (c->sticky != MOE_OK) return c->sticky;
+  if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(c);
+  uint32_t st = 0;
+  if (cudaMemcpy(&st, c->d_status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_fail(c);
+  if (st & ST_TIMEOUT) c->sticky = MOE_ETIMEOUT;
+  else if (st) c->sticky = MOE_ECUDA;
+  return c->sticky;
+}
+
+uint8_t* record_ptr_resident(moe_ctx* c, int layer, int expert) {
+  const int e = expert < 0 ? c->cfg.num_experts : expert;
+  return c->d_slab + ((size_t)layer * c->E1 + e) * c->rec_bytes;
+}
+
+void free_all(moe_ctx* c) {
+  cudaFree(c->d_slab);
+  cudaFree(c->d_shared);
+  if (c->h_pool) cudaFreeHost(c->h_pool);
+  cudaFree(c->d_router);
+  cudaFree(c->d_rec_table);
+  if (c->h_table) cudaFreeHost(c->h_table);
+  cudaFree(c->d_order);
+  if (c->h_order) cudaFreeHost(c->h_order);
+  cudaFree(c->d_rpart);
+  cudaFree(c->d_ticket);
+  cudaFree(c->d_plan_mem);
+  cudaFree(c->d_store_idx);
+  cudaFree(c->d_store_w);
+  cudaFree(c->d_part_gu);
+  cudaFree(c->d_part_d);
+  cudaFree(c->d_status);
+  cudaFree(c->d_dbg_status);
+  cudaFree(c->d_counters);
+  if (c->h_rb) cudaFreeHost(c->h_rb);
+  for (auto ev : c->copy_ev) cudaEventDestroy(ev);
+  if (c->side) cudaStreamDestroy(c->side);
+  if (c->reg) cudaStreamDestroy(c->reg);
+  cudaFree(c->d_blob_stage);
+  cudaFree(c->d_rec_stage);
+}
+
+moe_status validate(const moe_config* g) {
+  if (!g) return MOE_EINVAL;
+  if (g->num_layers < 1 || g->hidden < 8 || g->ffn < 8) return MOE_EINVAL;
+  if (g->num_experts < 1 || g->num_experts > 1024) return MOE_EINVAL;
+  if (g->top_k < 1 || g->top_k > g->num_experts || g->top_k > 32) return MOE_EINVAL;
+  if (g->shared_ffn != 0 && g->shared_ffn != g->ffn) return MOE_EINVAL;
+  if (g->router != MOE_ROUTER_SOFTMAX_TOPK_RENORM && g->router != MOE_ROUTER_SIGMOID_TOPK_NORM)
+    return MOE_EINVAL;
+  if (g->max_tokens < 1 || g->max_tokens > 256) return MOE_EINVAL;
+  if (g->wfmt == MOE_W_RVQ3_G8) {
+    if (g->hidden % 8 || g->ffn % 8) return MOE_EINVAL;
+  } else if (g->wfmt == MOE_W_INT4_G128) {
+    if (g->hidden % 128 || g->ffn % 128) return MOE_EINVAL;
+  } else {
+    return MOE_EINVAL;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_strerror(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_EINVAL: return "invalid argument";
+    case MOE_ENOMEM: return "out of memory (HBM or pinned host)";
+    case MOE_EBUDGET: return "expert cache below one layer's working set";
+    case MOE_ECUDA: return "CUDA error";
+    case MOE_ESTATE: return "layer not fully registered";
+    case MOE_ETIMEOUT: return "device wait timed out";
+    case MOE_ENOTFOUND: return "nothing recorded yet";
+  }
+  return "unknown status";
+}
+
+size_t moe_expert_blob_bytes(int wfmt, int hidden, int ffn) {
+  if (wfmt == MOE_W_RVQ3_G8) {
+    if (hidden <= 0 || ffn <= 0 || hidden % 8 || ffn % 8) return 0;
+  } else if (wfmt == MOE_W_INT4_G128) {
+    if (hidden <= 0 || ffn <= 0 || hidden % 128 || ffn % 128) return 0;
+  } else {
+    return 0;
+  }
+  return 2 * blob_matrix_bytes(wfmt, ffn, hidden) + blob_matrix_bytes(wfmt, hidden, ffn);
+}
+
+moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
+  if (!out) return MOE_EINVAL;
+  *out = nullptr;
+  moe_status v = validate(cfg);
+  if (v != MOE_OK) return v;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return ndev == 0 ? MOE_ECUDA : MOE_EINVAL;
+  }
+  DeviceGuard dg(device);
+  moe_ctx* c = new (std::nothrow) moe_ctx();
+  if (!c) return MOE_ENOMEM;
+  c->cfg = *cfg;
+  c->device = device;
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
+  const int L = cfg->num_layers, E = cfg->num_experts, H = cfg->hidden, F = cfg->ffn;
+  const int k = cfg->top_k, maxT = cfg->max_tokens;
+  c->has_shared = cfg->shared_ffn ? 1 : 0;
+  c->E1 = E + c->has_shared;
+  c->pmax = cfg->wfmt == MOE_W_INT4_G128 ? I4_PMAX : RVQ_PMAX;
+  c->rg = rec_geom(cfg->wfmt, H, F);
+  c->rec_bytes = c->rg.bytes;
+  c->blob_bytes = moe_expert_blob_bytes(cfg->wfmt, H, F);
+  c->streamed = cfg->hbm_cache_bytes != 0;
+  c->router_ok.assign(L, 0);
+  c->expert_ok.assign((size_t)L * c->E1, 0);
+  c->last_T.assign(L, -1);
+
+  // scratch geometry
+  c->max_pass = maxT * k + (c->has_shared ? maxT : 0);
+  const MatGeom& gg = c->rg.m[0];
+  const MatGeom& gd = c->rg.m[2];
+  const size_t part_gu = (size_t)c->max_pass * 2 * gg.nks * gg.ntask * 32 * c->pmax;
+  const size_t part_d = (size_t)c->max_pass * gd.nks * gd.ntask * 32 * c->pmax;
+  const size_t rpart = (size_t)E * router_nch(H) * maxT;
+  const size_t router_bytes = (size_t)L * E * H * sizeof(float);
+
+  size_t expert_bytes;
+  if (!c->streamed) {
+    expert_bytes = (size_t)L * c->E1 * c->rec_bytes;
+  } else {
+    size_t slots = cfg->hbm_cache_bytes / c->rec_bytes;
+    if (slots < (size_t)2 * k) {
+      delete c;
+      return MOE_EBUDGET;
+    }
+    slots = std::min(slots, (size_t)L * E);
+    c->n_slots = slots;
+    expert_bytes = slots * c->rec_bytes + (size_t)L * c->has_shared * c->rec_bytes;
+    const size_t pool = (size_t)L * E * c->rec_bytes;
+    const size_t avail = host_available_bytes();
+    if (pool + (8ull << 30) > avail) {
+      delete c;
+      return MOE_ENOMEM;
+    }
+  }
+  size_t free_b = 0, total_b = 0;
+  if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
+    delete c;
+    return MOE_ECUDA;
+  }
+  const size_t need = expert_bytes + router_bytes + (part_gu + part_d + rpart) * 4 +
+                      2 * c->blob_bytes + (64ull << 20);
+  if (need + (1ull << 30) > free_b) {
+    delete c;
+    return MOE_ENOMEM;
+  }
+
+#define AL(ptr, bytes)                                              \
+  do {                                                              \
+    if (cudaMalloc((void**)&(ptr), (bytes)) != cudaSuccess) {       \
+      cudaGetLastError();                                           \
+      free_all(c);                                                  \
+      delete c;                                                     \
+      return MOE_ENOMEM;                                            \
+    }                                                               \
+  } while (0)
+
+  if (!c->streamed) {
+    AL(c->d_slab, expert_bytes);
+    AL(c->d_rec_table, (size_t)L * (E + 1) * sizeof(uint8_t*));
+    std::vector<uint8_t*> tab((size_t)L * (E + 1));
+    for (int l = 0; l < L; ++l) {
+      for (int e = 0; e < E; ++e) tab[(size_t)l * (E + 1) + e] = record_ptr_resident(c, l, e);
+      tab[(size_t)l * (E + 1) + E] = c->has_shared ? record_ptr_resident(c, l, -1) : nullptr;
+    }
+    cudaMemcpy(c->d_rec_table, tab.data(), tab.size() * sizeof(uint8_t*), cudaMemcpyHostToDevice);
+  } else {
+    AL(c->d_slab, c->n_slots * c->rec_bytes);
+    if (c->has_shared) AL(c->d_shared, (size_t)L * c->rec_bytes);
+    AL(c->d_rec_table, (size_t)(E + 1) * sizeof(uint8_t*));
+    AL(c->d_order, (size_t)c->max_pass * sizeof(int));
+    if (cudaHostAlloc((void**)&c->h_pool, (size_t)L * E * c->rec_bytes, cudaHostAllocDefault) !=
+            cudaSuccess ||
+        cudaHostAlloc((void**)&c->h_table, (size_t)(E + 1) * sizeof(uint8_t*), cudaHostAllocDefault) !=
+            cudaSuccess ||
+        cudaHostAlloc((void**)&c->h_order, (size_t)c->max_pass * sizeof(int), cudaHostAllocDefault) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      free_all(c);
+      delete c;
+      return MOE_ENOMEM;
+    }
+    c->slot_key.assign(c->n_slots, -1);
+    c->lru_it.resize(c->n_slots);
+    c->slot_in_lru.assign(c->n_slots, 0);
+    c->slot_pinned.assign(c->n_slots, 0);
+    c->copy_ev.resize(E);
+    for (auto& ev : c->copy_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  }
+  if (cudaHostAlloc((void**)&c->h_rb, (size_t)(8 + E + c->max_pass) * sizeof(int),
+                    cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return MOE_ENOMEM;
+  }
+  AL(c->d_router, router_bytes);
+  AL(c->d_rpart, rpart * sizeof(float));
+  AL(c->d_ticket, sizeof(unsigned int));
+  AL(c->d_part_gu, part_gu * sizeof(float));
+  AL(c->d_part_d, part_d * sizeof(float));
+  AL(c->d_status, 4);
+  AL(c->d_dbg_status, 4);
+  AL(c->d_counters, sizeof(DevCounters));
+  AL(c->d_store_idx, (size_t)L * maxT * k * sizeof(int));
+  AL(c->d_store_w, (size_t)L * maxT * k * sizeof(float));
+  AL(c->d_blob_stage, c->blob_bytes);
+  AL(c->d_rec_stage, c->rec_bytes);
+  {
+    // plan arrays, one allocation
+    const size_t n_int = 16 + (size_t)c->max_pass * (2 + c->pmax) + (size_t)maxT * k * 4 +
+                         (size_t)maxT * 2 + E;
+    AL(c->d_plan_mem, n_int * sizeof(int));
+    int* p = (int*)c->d_plan_mem;
+    c->plan.hdr = (Plan*)p;
+    p += 16;
+    c->plan.pass_expert = p; p += c->max_pass;
+    c->plan.pass_ntok = p; p += c->max_pass;
+    c->plan.pass_tok = p; p += (size_t)c->max_pass * c->pmax;
+    c->plan.pair_pass = p; p += (size_t)maxT * k;
+    c->plan.pair_slot = p; p += (size_t)maxT * k;
+    c->plan.idx = p; p += (size_t)maxT * k;
+    c->plan.w = (float*)p; p += (size_t)maxT * k;
+    c->plan.shared_pass = p; p += maxT;
+    c->plan.shared_slot = p; p += maxT;
+    c->plan.uniq = p; p += E;
+  }
+#undef AL
+  cudaMemset(c->d_ticket, 0, sizeof(unsigned int));
+  cudaMemset(c->d_status, 0, 4);
+  cudaMemset(c->d_counters, 0, sizeof(DevCounters));
+  cudaMemset(c->d_plan_mem, 0, 16 * sizeof(int));
+  if (cudaStreamCreateWithFlags(&c->reg, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
+      router_set_attributes() != cudaSuccess || int4_set_attributes() != cudaSuccess ||
+      rvq_set_attributes() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return MOE_ECUDA;
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+moe_status moe_destroy(moe_ctx* c) {
+  if (!c) return MOE_OK;
+  {
+    DeviceGuard dg(c->device);
+    cudaDeviceSynchronize();
+    free_all(c);
+  }
+  delete c;
+  return MOE_OK;
+}
+
+moe_status moe_register_router(moe_ctx* c, int layer, const float* w) {
+  if (!c || !w || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
+  if (c->sticky != MOE_OK) return c->sticky;
+  DeviceGuard dg(c->device);
+  const size_t n = (size_t)c->cfg.num_experts * c->cfg.hidden;
+  float* dst = c->d_router + (size_t)layer * n;
+  CK(cudaMemcpy(dst, w, n * sizeof(float), is_device_ptr(w) ? cudaMemcpyDeviceToDevice
+                                                              : cudaMemcpyHostToDevice));
+  c->router_ok[layer] = 1;
+  return MOE_OK;
+}
+
+moe_status moe_register_expert(moe_ctx* c, int layer, int expert, const void* blob, size_t bytes) {
+  if (!c || !blob || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
+  if (expert < -1 || expert >= c->cfg.num_experts) return MOE_EINVAL;
+  if (expert == -1 && !c->has_shared) return MOE_EINVAL;
+  if (bytes != c->blob_bytes) return MOE_EINVAL;
+  if (c->sticky != MOE_OK) return c->sticky;
+  DeviceGuard dg(c->device);
+  const uint8_t* src = (const uint8_t*)blob;
+  if (!is_device_ptr(blob)) {
+    CK(cudaMemcpyAsync(c->d_blob_stage, blob, bytes, cudaMemcpyHostToDevice, c->reg));
+    src = c->d_blob_stage;
+  }
+  const int E = c->cfg.num_experts;
+  uint8_t* dst;
+  if (!c->streamed) dst = record_ptr_resident(c, layer, expert);
+  else if (expert < 0) dst = c->d_shared + (size_t)layer * c->rec_bytes;
+  else dst = c->d_rec_stage;
+  CK(launch_repack(c->cfg.wfmt, src, c->cfg.hidden, c->cfg.ffn, dst, c->reg));
+  if (c->streamed && expert >= 0) {
+    uint8_t* pool = c->h_pool + ((size_t)layer * E + expert) * c->rec_bytes;
+    CK(cudaMemcpyAsync(pool, dst, c->rec_bytes, cudaMemcpyDeviceToHost, c->reg));
+    // a stale cached copy of this expert must not survive re-registration
+    const long long key = (long long)layer * E + expert;
+    auto it = c->where.find(key);
+    if (it != c->where.end()) {
+      const int s = it->second;
+      if (c->slot_in_lru[s]) { c->lru.erase(c->lru_it[s]); c->slot_in_lru[s] = 0; }
+      c->slot_key[s] = -1;
+      c->where.erase(it);
+    }
+  }
+  CK(cudaStreamSynchronize(c->reg));
+  c->expert_ok[(size_t)layer * c->E1 + (expert < 0 ? E : expert)] = 1;
+  return MOE_OK;
+}
+
+static moe_status layer_ready(moe_ctx* c, int layer) {
+  if (!c->router_ok[layer]) return MOE_ESTATE;
+  for (int e = 0; e < c->E1; ++e)
+    if (!c->expert_ok[(size_t)layer * c->E1 + e]) return MOE_ESTATE;
+  return MOE_OK;
+}
+
+static ExpertArgs expert_args(moe_ctx* c, uint8_t* const* table, const void* x, int T) {
+  ExpertArgs a{};
+  a.rec_table = table;
+  a.plan = c->plan;
+  a.H = c->cfg.hidden;
+  a.F = c->cfg.ffn;
+  a.E = c->cfg.num_experts;
+  a.T = T;
+  a.x = (const uint16_t*)x;
+  a.part_gu = c->d_part_gu;
+  a.part_d = c->d_part_d;
+  a.range.order = nullptr;
+  a.range.p_begin = 0;
+  a.range.p_end = -1;
+  a.status = c->d_status;
+  a.budget = c->budget;
+  return a;
+}
+
+static cudaError_t launch_experts(moe_ctx* c, const ExpertArgs& a, cudaStream_t s) {
+  cudaError_t e;
+  if (c->cfg.wfmt == MOE_W_INT4_G128) {
+    e = launch_int4_gateup(a, c->num_sms, s);
+    if (e == cudaSuccess) e = launch_int4_down(a, c->num_sms, s);
+  } else {
+    e = launch_rvq_gateup(a, c->num_sms, s);
+    if (e == cudaSuccess) e = launch_rvq_down(a, c->num_sms, s);
+  }
+  return e;
+}
+
+// LRU: find or make a slot for `key`; returns slot and whether it was a hit.
+static int cache_get(moe_ctx* c, long long key, bool* hit) {
+  auto it = c->where.find(key);
+  if (it != c->where.end()) {
+    const int s = it->second;
+    if (c->slot_in_lru[s]) c->lru.erase(c->lru_it[s]);
+    c->lru.push_front(s);
+    c->lru_it[s] = c->lru.begin();
+    c->slot_in_lru[s] = 1;
+    *hit = true;
+    return s;
+  }
+  *hit = false;
+  int s = -1;
+  // an empty slot first, else the least recently used unpinned one
+  if (c->where.size() < c->n_slots) {
+    for (size_t i = 0; i < c->n_slots; ++i)
+      if (c->slot_key[i] < 0) { s = (int)i; break; }
+  }
+  if (s < 0) {
+    for (auto r = c->lru.rbegin(); r != c->lru.rend(); ++r)
+      if (!c->slot_pinned[*r]) { s = *r; break; }
+    if (s < 0) return -1;
+    c->where.erase(c->slot_key[s]);
+    c->lru.erase(c->lru_it[s]);
+    c->slot_in_lru[s] = 0;
+  }
+  c->slot_key[s] = key;
+  c->where[key] = s;
+  c->lru.push_front(s);
+  c->lru_it[s] = c->lru.begin();
+  c->slot_in_lru[s] = 1;
+  return s;
+}
+
+moe_status moe_forward(moe_ctx* c, int layer, const void* x, float* out, int T, void* stream) {
+  if (!c || !x || !out || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
+  if (T < 1 || T > c->cfg.max_tokens) return MOE_EINVAL;
+  if (c->sticky != MOE_OK) return c->sticky;
+  moe_status rs = layer_ready(c, layer);
+  if (rs != MOE_OK) return rs;
+  DeviceGuard dg(c->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int L = c->cfg.num_layers, E = c->cfg.num_experts, H = c->cfg.hidden, k = c->cfg.top_k;
+  (void)L;
+
+  RouterArgs ra{};
+  ra.x = (const uint16_t*)x;
+  ra.W = c->d_router + (size_t)layer * E * H;
+  ra.T = T;
+  ra.H = H;
+  ra.E = E;
+  ra.k = k;
+  ra.kind = c->cfg.router;
+  ra.pmax = c->pmax;
+  ra.has_shared = c->has_shared;
+  ra.partial = c->d_rpart;
+  ra.ticket = c->d_ticket;
+  ra.plan = c->plan;
+  ra.store_idx = c->d_store_idx + (size_t)layer * c->cfg.max_tokens * k;
+  ra.store_w = c->d_store_w + (size_t)layer * c->cfg.max_tokens * k;
+  ra.counters = c->d_counters;
+  ra.record_bytes = c->rec_bytes;
+  CK(launch_router(ra, c->num_sms, s));
+
+  CombineArgs ca{};
+  ca.plan = c->plan;
+  ca.part_d = c->d_part_d;
+  ca.T = T;
+  ca.H = H;
+  ca.k = k;
+  ca.pmax = c->pmax;
+  ca.nks_d = c->rg.m[2].nks;
+  ca.has_shared = c->has_shared;
+  ca.out = out;
+
+  if (!c->streamed) {
+    ExpertArgs a = expert_args(c, c->d_rec_table + (size_t)layer * (E + 1), x, T);
+    CK(launch_experts(c, a, s));
+    CK(launch_combine(ca, s));
+    c->last_T[layer] = T;
+    return MOE_OK;
+  }
+
+  // ---------------- streamed: read the plan back (the one host round trip per layer)
+  int* rb = c->h_rb;
+  CK(cudaMemcpyAsync(rb, c->plan.hdr, 4 * sizeof(int), cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(rb + 8, c->plan.uniq, (size_t)E * sizeof(int), cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(rb + 8 + E, c->plan.pass_expert, (size_t)c->max_pass * sizeof(int),
+                     cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  {
+    uint32_t st = 0;
+    CK(cudaMemcpy(&st, c->d_status, 4, cudaMemcpyDeviceToHost));
+    if (st) {
+      c->sticky = (st & ST_TIMEOUT) ? MOE_ETIMEOUT : MOE_ECUDA;
+      return c->sticky;
+    }
+  }
+  const int n_pass = rb[0], n_uniq = rb[1], n_routed = rb[2];
+  const int* uniq = rb + 8;
+  const int* pexp = rb + 8 + E;
+
+  for (size_t i = 0; i < c->n_slots; ++i) c->slot_pinned[i] = 0;
+  std::vector<int> miss_experts;
+  std::vector<char> is_miss(E, 0);
+  for (int i = 0; i < n_uniq; ++i) {
+    const int e = uniq[i];
+    bool hit = false;
+    const int slot = cache_get(c, (long long)layer * E + e, &hit);
+    if (slot < 0) return MOE_EBUDGET;  // cannot happen: slots >= 2k >= unique experts
+    c->slot_pinned[slot] = 1;
+    c->h_table[e] = c->d_slab + (size_t)slot * c->rec_bytes;
+    if (hit) {
+      ++c->hits;
+    } else {
+      ++c->misses;
+      is_miss[e] = 1;
+      miss_experts.push_back(e);
+    }
+  }
+  c->h_table[E] = c->has_shared ? c->d_shared + (size_t)layer * c->rec_bytes : nullptr;
+
+  // miss copies on the side stream, in ascending expert id, one event each
+  auto t_copy0 = std::chrono::steady_clock::now();
+  for (size_t m = 0; m < miss_experts.size(); ++m) {
+    const int e = miss_experts[m];
+    const uint8_t* src = c->h_pool + ((size_t)layer * E + e) * c->rec_bytes;
+    cudaError_t ce;
+    if (c->fail_copies > 0) {
+      --c->fail_copies;
+      ce = cudaErrorInvalidValue;  // injected failure of the copy call
+    } else {
+      ce = cudaMemcpyAsync(c->h_table[e], src, c->rec_bytes, cudaMemcpyHostToDevice, c->side);
+    }
+    if (ce != cudaSuccess) {
+      // the slot's content is unknown now: forget it
+      c->where.erase((long long)layer * E + e);
+      for (size_t i = 0; i < c->n_slots; ++i)
+        if (c->slot_key[i] == (long long)layer * E + e) {
+          c->slot_key[i] = -1;
+          if (c->slot_in_lru[i]) { c->lru.erase(c->lru_it[i]); c->slot_in_lru[i] = 0; }
+        }
+      return cuda_fail(c);
+    }
+    CK(cudaEventRecord(c->copy_ev[m], c->side));
+    c->bytes_h2d += c->rec_bytes;
+  }
+
+  // pass order: hits (and the shared expert) first, then each miss's passes
+  int n_first = 0;
+  for (int p = 0; p < n_pass; ++p) {
+    const bool shared_pass = p >= n_routed;
+    if (shared_pass || !is_miss[pexp[p]]) c->h_order[n_first++] = p;
+  }
+  std::vector<int> miss_begin(miss_experts.size() + 1);
+  int pos = n_first;
+  for (size_t m = 0; m < miss_experts.size(); ++m) {
+    miss_begin[m] = pos;
+    for (int p = 0; p < n_routed; ++p)
+      if (pexp[p] == miss_experts[m]) c->h_order[pos++] = p;
+  }
+  miss_begin[miss_experts.size()] = pos;
+  CK(cudaMemcpyAsync(c->d_rec_table, c->h_table, (size_t)(E + 1) * sizeof(uint8_t*),
+                     cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(c->d_order, c->h_order, (size_t)n_pass * sizeof(int), cudaMemcpyHostToDevice, s));
+
+  ExpertArgs a = expert_args(c, c->d_rec_table, x, T);
+  a.range.order = c->d_order;
+  if (n_first > 0) {
+    a.range.p_begin = 0;
+    a.range.p_end = n_first;
+    CK(launch_experts(c, a, s));
+  }
+  for (size_t m = 0; m < miss_experts.size(); ++m) {
+    CK(cudaStreamWaitEvent(s, c->copy_ev[m], 0));
+    a.range.p_begin = miss_begin[m];
+    a.range.p_end = miss_begin[m + 1];
+    CK(launch_experts(c, a, s));
+  }
+  CK(launch_combine(ca, s));
+  if (!miss_experts.empty()) {
+    // wall time of the copies as seen by the host (the side stream is otherwise idle)
+    CK(cudaEventSynchronize(c->copy_ev[miss_experts.size() - 1]));
+    c->h2d_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_copy0).count();
+  }
+  c->last_T[layer] = T;
+  return MOE_OK;
+}
+
+moe_status moe_get_routing(moe_ctx* c, int layer, int* idx, float* w, int* T_out) {
+  if (!c || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
+  DeviceGuard dg(c->device);
+  moe_status st = check_device(c);
+  if (st != MOE_OK) return st;
+  const int T = c->last_T[layer];
+  if (T_out) *T_out = T < 0 ? 0 : T;
+  if (T < 0) return MOE_ENOTFOUND;
+  const size_t n = (size_t)T * c->cfg.top_k;
+  const size_t off = (size_t)layer * c->cfg.max_tokens * c->cfg.top_k;
+  if (idx) CK(cudaMemcpy(idx, c->d_store_idx + off, n * sizeof(int), cudaMemcpyDeviceToHost));
+  if (w) CK(cudaMemcpy(w, c->d_store_w + off, n * sizeof(float), cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+moe_status moe_residual_rmsnorm(moe_ctx* c, float* x, const float* y, uint16_t* xn, int T, float eps,
+                                void* stream) {
+  if (!c || !x || !xn || T < 1) return MOE_EINVAL;
+  if (c->sticky != MOE_OK) return c->sticky;
+  DeviceGuard dg(c->device);
+  CK(launch_residual_rmsnorm(x, y, xn, T, c->cfg.hidden, eps, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_stats(moe_ctx* c, moe_stats_t* out) {
+  if (!c || !out) return MOE_EINVAL;
+  DeviceGuard dg(c->device);
+  moe_status st = check_device(c);
+  DevCounters dc{};
+  if (cudaMemcpy(&dc, c->d_counters, sizeof(dc), cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_fail(c);
+  memset(out, 0, sizeof(*out));
+  out->forwards = dc.forwards;
+  out->tokens = dc.tokens;
+  out->lookups = dc.lookups;
+  out->hits = c->streamed ? c->hits : dc.lookups;
+  out->misses = c->streamed ? c->misses : 0;
+  out->bytes_expert_touched = dc.bytes_touched;
+  out->bytes_router = dc.bytes_router;
+  out->bytes_h2d = c->bytes_h2d;
+  out->record_bytes = c->rec_bytes;
+  out->cache_slots = c->n_slots;
+  out->h2d_ms = c->h2d_ms;
+  return st;
+}
+
+moe_status moe_reset_stats(moe_ctx* c) {
+  if (!c) return MOE_EINVAL;
+  DeviceGuard dg(c->device);
+  moe_status st = check_device(c);
+  if (st != MOE_OK) return st;
+  CK(cudaMemset(c->d_counters, 0, sizeof(DevCounters)));
+  c->hits = c->misses = c->bytes_h2d = 0;
+  c->h2d_ms = 0.0;
+  return MOE_OK;
+}
+
+moe_status moe_debug_fail_copies(moe_ctx* c, int n) {
+  if (!c || n < 0) return MOE_EINVAL;
+  c->fail_copies = n;
+  return MOE_OK;
+}
+
+moe_status moe_debug_wait_timeout(moe_ctx* c, unsigned long long cycles, void* stream, int* status) {
+  if (!c || !status) return MOE_EINVAL;
+  DeviceGuard dg(c->device);
+  CK(cudaMemsetAsync(c->d_dbg_status, 0, 4, (cudaStream_t)stream));
+  CK(launch_wait_timeout(c->d_dbg_status, cycles, (cudaStream_t)stream));
+  uint32_t st = 0;
+  CK(cudaMemcpyAsync(&st, c->d_dbg_status, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream));
+  CK(cudaStreamSynchronize((cudaStream_t)stream));
+  *status = (st & ST_TIMEOUT) ? MOE_ETIMEOUT : (st ? MOE_ECUDA : MOE_OK);
+  return MOE_OK;
+}
+
+}  // extern "C"

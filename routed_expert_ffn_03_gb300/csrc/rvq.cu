@@ -1,0 +1,241 @@
+// rvq.cu - residual-VQ (3 stages x 256 x 8 fp16 codebooks, 3 bits/weight) expert GEMV.
+//
+// "2.78T-parameter model on a laptop: the NVMe streaming inference engine WASTE",
+// section "Idle weights only need to arrive on time": experts are stored residual-vector
+// quantised at 3.00 bits per weight and the matrices are never expanded.  Here they are
+// not expanded either: for a token x and one k-slice of 64 groups, the block first
+// builds the table
+//     LUT[s][c][q] = sum_i C_s[c][i] * x[8q + i]     (s < 3, c < 256, q < 64)
+// in fp32 (192 KB of shared memory), and then every output row is
+//     y[r] = sum_q LUT[0][c0(r,q)][q] + LUT[1][c1(r,q)][q] + LUT[2][c2(r,q)][q]
+// which equals sum_k W[r][k] x[k] for W[r][8q+i] = C0[c0][i] + C1[c1][i] + C2[c2][i].
+//
+// Table build: D[q][e] = X[q][.] . Cb[e][.] is a [64 x 8] x [8 x 768] product done with
+// m16n8k8 tensor-core mma (the fp16 codebook entries are used as stored; the fp32 input
+// is split into fp16 hi + lo, two mma into one fp32 accumulator).  Each lane then writes
+// its accumulators in a rotated order so that one store instruction touches 32 banks.
+//
+// Lookups: lane l owns row 32*block + l and visits the 64 groups in the order
+// q = l XOR i (i = 0..63); the table is laid out [s][c][q] with 64 words per (s, c), so
+// the bank of a lookup is q mod 32 and the 32 lanes hit 32 different banks whatever
+// their codes.  The codes are read with 16-byte streaming loads straight into registers
+// (one task = 32 rows x 64 groups = 6144 contiguous bytes), the next task's loads in
+// flight while the current one is summed.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int RV_NW = 8;                               // warps per block
+constexpr int RV_LUT_BYTES = 3 * 256 * RVQ_KS * 4;     // 196608
+constexpr int RV_VIN_BYTES = RVQ_KS * RVQ_GROUP * 4;   // 2048
+constexpr int RV_SMEM = RV_LUT_BYTES + RV_VIN_BYTES;
+constexpr int RV_WQ = RVQ_TASK_BYTES / 512;            // 12 uint4 per lane per task
+
+template <int OFF>
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
+
+struct RvUnit {
+  int pass, m, ks, expert;
+  const uint8_t* base;   // matrix base (codebooks first)
+};
+
+template <bool DOWN>
+__device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, long long u, int nks, int p_begin,
+                                          const RecGeom& rg) {
+  constexpr int mats = DOWN ? 1 : 2;
+  RvUnit U;
+  U.ks = (int)(u % nks);
+  const long long pm = u / nks;
+  U.m = (int)(pm % mats);
+  const int pi = (int)(pm / mats);
+  U.pass = a.range.order ? a.range.order[p_begin + pi] : p_begin + pi;
+  U.expert = a.plan.pass_expert[U.pass];
+  U.base = a.rec_table[U.expert] + (DOWN ? rg.off[2] : (U.m == 0 ? rg.off[0] : rg.off[1]));
+  return U;
+}
+
+__device__ __forceinline__ void load_task(uint4 (&v)[RV_WQ], const uint8_t* p, int lane) {
+#pragma unroll
+  for (int j = 0; j < RV_WQ; ++j) v[j] = ldg_stream(p + (j * 32 + lane) * 16);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 (&v)[RV_WQ], int w) {
+  const uint4& q = v[w >> 2];
+  return (w & 3) == 0 ? q.x : (w & 3) == 1 ? q.y : (w & 3) == 2 ? q.z : q.w;
+}
+
+// Sum of the 64 groups' three lookups for this lane's row.
+__device__ __forceinline__ float rvq_row_sum(const uint4 (&v)[RV_WQ], uint32_t lut, uint32_t l4) {
+  float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f;
+#pragma unroll
+  for (int c4 = 0; c4 < 16; ++c4) {
+    const uint32_t w0 = word_of(v, 3 * c4), w1 = word_of(v, 3 * c4 + 1), w2 = word_of(v, 3 * c4 + 2);
+    // group positions i = 4 c4 + u; code bytes (stage 0,1,2) at stream bytes 3i..3i+2
+    const uint32_t q0 = l4 ^ (uint32_t)((4 * c4 + 0) << 2);
+    const uint32_t q1 = l4 ^ (uint32_t)((4 * c4 + 1) << 2);
+    const uint32_t q2 = l4 ^ (uint32_t)((4 * c4 + 2) << 2);
+    const uint32_t q3 = l4 ^ (uint32_t)((4 * c4 + 3) << 2);
+    // prmt: byte 1 <- code byte, byte 0 <- qoff, bytes 2,3 <- 0  => (c << 8) | 4q
+    acc0 += lds_f32<0>(lut + prmt(w0, q0, 0x5504));
+    acc1 += lds_f32<65536>(lut + prmt(w0, q0, 0x5514));
+    acc2 += lds_f32<131072>(lut + prmt(w0, q0, 0x5524));
+    acc0 += lds_f32<0>(lut + prmt(w0, q1, 0x5534));
+    acc1 += lds_f32<65536>(lut + prmt(w1, q1, 0x5504));
+    acc2 += lds_f32<131072>(lut + prmt(w1, q1, 0x5514));
+    acc0 += lds_f32<0>(lut + prmt(w1, q2, 0x5524));
+    acc1 += lds_f32<65536>(lut + prmt(w1, q2, 0x5534));
+    acc2 += lds_f32<131072>(lut + prmt(w2, q2, 0x5504));
+    acc0 += lds_f32<0>(lut + prmt(w2, q3, 0x5514));
+    acc1 += lds_f32<65536>(lut + prmt(w2, q3, 0x5524));
+    acc2 += lds_f32<131072>(lut + prmt(w2, q3, 0x5534));
+  }
+  return (acc0 + acc1) + acc2;
+}
+
+template <bool DOWN>
+__global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* lutf = reinterpret_cast<float*>(smem);
+  float* vin = reinterpret_cast<float*>(smem + RV_LUT_BYTES);
+  const uint32_t lut = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, p = lane & 3;
+  constexpr int mats = DOWN ? 1 : 2;
+  const RecGeom rg = rec_geom(WFMT_RVQ, a.H, a.F);
+  const MatGeom g = rg.m[DOWN ? 2 : 0];
+  const MatGeom gg = rg.m[0];
+  const int nks = g.nks, ntask = g.ntask;
+  const int rows32 = ntask * 32, rows32_gu = gg.ntask * 32;
+  const int p_begin = a.range.p_begin;
+  const int p_end = a.range.p_end < 0 ? a.plan.hdr->n_pass : a.range.p_end;
+  const long long total = (long long)max(0, p_end - p_begin) * mats * nks * ntask;
+  const long long t0 = total * blockIdx.x / gridDim.x;
+  const long long t1 = total * (blockIdx.x + 1) / gridDim.x;
+  const uint32_t l4 = (uint32_t)lane << 2;
+
+  for (long long i = t0; i < t1;) {
+    const long long u = i / ntask;
+    const long long seg_end = min(t1, (u + 1) * ntask);
+    const RvUnit U = rv_unit<DOWN>(a, u, nks, p_begin, rg);
+    const uint8_t* codes = U.base + RVQ_CB_BYTES + (size_t)U.ks * ntask * RVQ_TASK_BYTES;
+
+    // first task's codes go in flight before the table is built
+    long long ti = i + warp;
+    uint4 va[RV_WQ], vb[RV_WQ];
+    if (ti < seg_end) load_task(va, codes + (size_t)(ti % ntask) * RVQ_TASK_BYTES, lane);
+
+    __syncthreads();  // the previous unit's table is no longer read
+    {
+      const int tok = a.plan.pass_tok[U.pass];   // one token per pass
+      const int kbase = U.ks * RVQ_KS * RVQ_GROUP;
+      for (int e = threadIdx.x; e < RVQ_KS * RVQ_GROUP; e += RV_NW * 32) {
+        const int k = kbase + e;
+        float v = 0.f;
+        if (k < g.K) {
+          if (!DOWN) {
+            v = bf16_bits_to_float(a.x[(size_t)tok * a.H + k]);
+          } else {
+            const float* pg = a.part_gu + ((size_t)(U.pass * 2 + 0) * gg.nks) * rows32_gu + k;
+            const float* pu = a.part_gu + ((size_t)(U.pass * 2 + 1) * gg.nks) * rows32_gu + k;
+            float gs = 0.f, us = 0.f;
+#pragma unroll 4
+            for (int s2 = 0; s2 < gg.nks; ++s2) {
+              gs += __ldcg(pg + (size_t)s2 * rows32_gu);
+              us += __ldcg(pu + (size_t)s2 * rows32_gu);
+            }
+            v = gs / (1.f + expf(-gs)) * us;
+          }
+        }
+        vin[e] = v;
+      }
+    }
+    __syncthreads();
+    {
+      // A fragments: rows = groups q, k = element i (hi and lo parts)
+      uint32_t ahi[4][2], alo[4][2];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q = 16 * mt + gq + 8 * h;
+          __half h0, l0, h1, l1;
+          split_half(vin[q * 8 + 2 * p], h0, l0);
+          split_half(vin[q * 8 + 2 * p + 1], h1, l1);
+          ahi[mt][h] = pack_half2(h0, h1);
+          alo[mt][h] = pack_half2(l0, l1);
+        }
+      }
+      const uint32_t* cb = reinterpret_cast<const uint32_t*>(U.base);  // fp16 [768][8]
+      for (int nt = warp; nt < 96; nt += RV_NW) {
+        const int e0 = nt * 8;
+        const uint32_t b = __ldg(cb + (e0 + gq) * 4 + p);
+#pragma unroll
+        for (int P = 0; P < 2; ++P) {
+          float dA[4] = {0.f, 0.f, 0.f, 0.f}, dB[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_1688(dA, ahi[2 * P][0], ahi[2 * P][1], b);
+          mma_1688(dA, alo[2 * P][0], alo[2 * P][1], b);
+          mma_1688(dB, ahi[2 * P + 1][0], ahi[2 * P + 1][1], b);
+          mma_1688(dB, alo[2 * P + 1][0], alo[2 * P + 1][1], b);
+          // value j of entry e: q = 32P + g + 8j  (j: A row g, A row g+8, B row g, B row g+8)
+          float* row0 = lutf + (size_t)(e0 + 2 * p) * RVQ_KS + 32 * P + gq;
+          float* row1 = row0 + RVQ_KS;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = (p + r) & 3;
+            const float v0 = j == 0 ? dA[0] : j == 1 ? dA[2] : j == 2 ? dB[0] : dB[2];
+            const float v1 = j == 0 ? dA[1] : j == 1 ? dA[3] : j == 2 ? dB[1] : dB[3];
+            row0[8 * j] = v0;
+            row1[8 * j] = v1;
+          }
+        }
+      }
+    }
+    __syncthreads();
+
+    // tasks of this unit: warp-strided, two register buffers
+    const size_t out_base = DOWN ? ((size_t)U.pass * nks + U.ks) * rows32
+                                 : ((size_t)(U.pass * 2 + U.m) * nks + U.ks) * rows32;
+    float* outp = DOWN ? a.part_d : a.part_gu;
+    while (ti < seg_end) {
+      const long long tn = ti + RV_NW;
+      if (tn < seg_end) load_task(vb, codes + (size_t)(tn % ntask) * RVQ_TASK_BYTES, lane);
+      {
+        const float y = rvq_row_sum(va, lut, l4);
+        outp[out_base + (size_t)(ti % ntask) * 32 + lane] = y;
+      }
+      ti = tn;
+      if (ti >= seg_end) break;
+      const long long tn2 = ti + RV_NW;
+      if (tn2 < seg_end) load_task(va, codes + (size_t)(tn2 % ntask) * RVQ_TASK_BYTES, lane);
+      {
+        const float y = rvq_row_sum(vb, lut, l4);
+        outp[out_base + (size_t)(ti % ntask) * 32 + lane] = y;
+      }
+      ti = tn2;
+    }
+    i = seg_end;
+  }
+}
+
+cudaError_t rvq_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(rvq_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, RV_SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(rvq_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, RV_SMEM);
+}
+
+cudaError_t launch_rvq_gateup(const ExpertArgs& a, int grid, cudaStream_t s) {
+  rvq_kernel<false><<<grid, RV_NW * 32, RV_SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+cudaError_t launch_rvq_down(const ExpertArgs& a, int grid, cudaStream_t s) {
+  rvq_kernel<true><<<grid, RV_NW * 32, RV_SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

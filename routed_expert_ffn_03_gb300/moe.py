@@ -1,0 +1,202 @@
+"""Python binding of the C ABI in include/moe.h (argument marshalling only).
+
+Every step of the layer runs in ``libmoe.so``'s CUDA kernels; PyTorch provides device
+memory and streams.  The library is built in-tree by ``build.py``; importing this module
+fails loudly if it is missing or cannot be loaded (there is no CPU fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIBMOE = os.path.join(PKG, "libmoe.so")
+
+OK, EINVAL, ENOMEM, EBUDGET, ECUDA, ESTATE, ETIMEOUT, ENOTFOUND = range(8)
+ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
+W_RVQ3, W_INT4 = 1, 2
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, strerror(status), status))
+
+
+class Config(ctypes.Structure):
+    _fields_ = [
+        ("num_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("ffn", ctypes.c_int),
+        ("num_experts", ctypes.c_int), ("top_k", ctypes.c_int), ("shared_ffn", ctypes.c_int),
+        ("router", ctypes.c_int), ("wfmt", ctypes.c_int), ("max_tokens", ctypes.c_int),
+        ("hbm_cache_bytes", ctypes.c_ulonglong),
+    ]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_ulonglong) for n in (
+        "forwards", "tokens", "lookups", "hits", "misses", "bytes_expert_touched",
+        "bytes_router", "bytes_h2d", "record_bytes", "cache_slots")] + [("h2d_ms", ctypes.c_double)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+
+
+def lib():
+    """Load libmoe.so (raises if it is missing: build it with build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBMOE):
+        raise RuntimeError("libmoe.so is not built (%s); run routed_expert_ffn_03_gb300.build.build()" % LIBMOE)
+    L = ctypes.CDLL(LIBMOE)
+    vp, i, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong
+    L.moe_create.argtypes = [ctypes.POINTER(Config), i, ctypes.POINTER(vp)]
+    L.moe_register_router.argtypes = [vp, i, vp]
+    L.moe_register_expert.argtypes = [vp, i, i, vp, ctypes.c_size_t]
+    L.moe_expert_blob_bytes.argtypes = [i, i, i]
+    L.moe_expert_blob_bytes.restype = ctypes.c_size_t
+    L.moe_forward.argtypes = [vp, i, vp, vp, i, vp]
+    L.moe_get_routing.argtypes = [vp, i, vp, vp, ctypes.POINTER(i)]
+    L.moe_residual_rmsnorm.argtypes = [vp, vp, vp, vp, i, ctypes.c_float, vp]
+    L.moe_stats.argtypes = [vp, ctypes.POINTER(Stats)]
+    L.moe_reset_stats.argtypes = [vp]
+    L.moe_destroy.argtypes = [vp]
+    L.moe_strerror.argtypes = [i]
+    L.moe_strerror.restype = ctypes.c_char_p
+    L.moe_debug_fail_copies.argtypes = [vp, i]
+    L.moe_debug_wait_timeout.argtypes = [vp, u64, vp, ctypes.POINTER(i)]
+    for name in ("moe_create", "moe_register_router", "moe_register_expert", "moe_forward",
+                 "moe_get_routing", "moe_residual_rmsnorm", "moe_stats", "moe_reset_stats",
+                 "moe_destroy", "moe_debug_fail_copies", "moe_debug_wait_timeout"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def strerror(status: int) -> str:
+    return lib().moe_strerror(status).decode()
+
+
+def expert_blob_bytes(wfmt: int, hidden: int, ffn: int) -> int:
+    return int(lib().moe_expert_blob_bytes(wfmt, hidden, ffn))
+
+
+def _ptr(t):
+    """Address of a torch tensor or numpy array (or an int address)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    return t.ctypes.data
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Context:
+    """One stack of MoE layers on one GPU (wraps moe_ctx)."""
+
+    def __init__(self, num_layers, hidden, ffn, num_experts, top_k, wfmt, router=ROUTER_SOFTMAX,
+                 shared_ffn=0, max_tokens=1, hbm_cache_bytes=0, device=0):
+        self.cfg = Config(num_layers, hidden, ffn, num_experts, top_k, shared_ffn, router, wfmt,
+                          max_tokens, hbm_cache_bytes)
+        self.device = device
+        h = ctypes.c_void_p()
+        st = lib().moe_create(ctypes.byref(self.cfg), device, ctypes.byref(h))
+        if st != OK:
+            raise MoeError(st, "moe_create")
+        self._h = h
+
+    # -- lifetime
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().moe_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, st, what):
+        if st != OK:
+            raise MoeError(st, what)
+
+    # -- registration
+    def register_router(self, layer, w):
+        """w: fp32 [E, H] (numpy array or torch tensor, host or this device)."""
+        self._check(lib().moe_register_router(self._h, layer, _ptr(w)), "moe_register_router")
+
+    def register_expert(self, layer, expert, blob, nbytes=None):
+        """blob: uint8 boundary-format blob (numpy/torch, host or device); expert -1 = shared."""
+        if nbytes is None:
+            nbytes = blob.numel() if hasattr(blob, "numel") else blob.nbytes
+        self._check(lib().moe_register_expert(self._h, layer, expert, _ptr(blob), nbytes),
+                    "moe_register_expert")
+
+    # -- compute
+    def forward(self, layer, x_bf16, out, T=None, stream=None):
+        """x_bf16: int16/bfloat16 cuda tensor [T, H]; out: float32 cuda tensor [T, H]."""
+        if T is None:
+            T = x_bf16.shape[0]
+        self._check(lib().moe_forward(self._h, layer, _ptr(x_bf16), _ptr(out), T, _stream(stream)),
+                    "moe_forward")
+
+    def residual_rmsnorm(self, x, y, xn, T=None, eps=1e-6, stream=None):
+        if T is None:
+            T = x.shape[0]
+        self._check(lib().moe_residual_rmsnorm(self._h, _ptr(x), _ptr(y), _ptr(xn), T,
+                                               float(eps), _stream(stream)),
+                    "moe_residual_rmsnorm")
+
+    def get_routing(self, layer):
+        import numpy as np
+        k, maxT = self.cfg.top_k, self.cfg.max_tokens
+        idx = np.zeros((maxT, k), dtype=np.int32)
+        w = np.zeros((maxT, k), dtype=np.float32)
+        T = ctypes.c_int(0)
+        self._check(lib().moe_get_routing(self._h, layer, idx.ctypes.data, w.ctypes.data,
+                                          ctypes.byref(T)), "moe_get_routing")
+        return idx[:T.value].copy(), w[:T.value].copy()
+
+    def stats(self):
+        s = Stats()
+        self._check(lib().moe_stats(self._h, ctypes.byref(s)), "moe_stats")
+        return s.as_dict()
+
+    def stats_status(self):
+        """(status, stats) without raising: for tests of sticky errors."""
+        s = Stats()
+        st = lib().moe_stats(self._h, ctypes.byref(s))
+        return st, s.as_dict()
+
+    def reset_stats(self):
+        self._check(lib().moe_reset_stats(self._h), "moe_reset_stats")
+
+    # -- failure injection (host side)
+    def debug_fail_copies(self, n):
+        self._check(lib().moe_debug_fail_copies(self._h, n), "moe_debug_fail_copies")
+
+    def debug_wait_timeout(self, cycles, stream=None):
+        st = ctypes.c_int(-1)
+        self._check(lib().moe_debug_wait_timeout(self._h, cycles, _stream(stream), ctypes.byref(st)),
+                    "moe_debug_wait_timeout")
+        return st.value

@@ -1,0 +1,69 @@
+"""GPU parity of the whole layer (C ABI) against the fp64 oracle, small shapes.
+
+Shapes span several tiles and ragged tails: rows not multiples of 32, k-slices with
+fewer groups than the tile, E below and above 32 / 256, T = 1, 3, 4, 32, both router
+kinds, the shared expert, both weight formats.
+"""
+import numpy as np
+import pytest
+
+import synth as S
+from tests.helpers import LayerSpec, compare, gpu_forward, make_context, oracle_forward, x_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from routed_expert_ffn_03_gb300 import build
+    build.build()
+
+
+def _run(spec, T, stream_id=0):
+    ctx = make_context(spec, max_tokens=T)
+    try:
+        xb = x_tokens(spec.seed + 100, stream_id, T, spec.H)
+        y, idx, w = gpu_forward(ctx, 0, xb)
+        ref = oracle_forward(spec, 0, xb)
+        return compare(ref, y, idx, w)
+    finally:
+        ctx.close()
+
+
+def test_tiny_config_rvq_top2_softmax():
+    """1 layer, H=256, F=512, 8 experts, top-2 softmax renormalised, T=4, RVQ-3bit."""
+    r = _run(LayerSpec(256, 512, 8, 2, S.RVQ, router=0, seed=0), T=4)
+    assert r["tokens"] == 4
+
+
+@pytest.mark.parametrize("H,F,E,k,T,router,shared", [
+    (72, 40, 5, 2, 1, 0, False),        # rows and K far below one tile
+    (264, 200, 33, 3, 3, 1, True),      # ragged k-slice (33 groups), E > 32, sigmoid + shared
+    (520, 96, 7, 7, 4, 0, False),       # k = E
+    (128, 64, 300, 8, 2, 1, False),     # E > 256
+    (256, 136, 16, 4, 32, 0, True),     # T = 32 with shared expert
+])
+def test_rvq_odd_shapes(H, F, E, k, T, router, shared):
+    _run(LayerSpec(H, F, E, k, S.RVQ, router=router, shared=shared, seed=H + F + E), T)
+
+
+@pytest.mark.parametrize("H,F,E,k,T,router,shared", [
+    (128, 128, 4, 2, 1, 0, False),      # one group per row
+    (384, 640, 6, 2, 1, 0, False),      # 3 and 5 groups: ragged 4-group k-slices
+    (512, 384, 9, 3, 3, 1, True),       # sigmoid + shared, T = 3
+    (256, 256, 40, 4, 4, 0, False),     # one pass carries 4 tokens when they share an expert
+    (256, 128, 8, 2, 32, 1, True),      # T = 32: experts with > 4 tokens take several passes
+])
+def test_int4_odd_shapes(H, F, E, k, T, router, shared):
+    _run(LayerSpec(H, F, E, k, S.INT4, router=router, shared=shared, seed=H + F + E), T)
+
+
+def test_device_generator_matches_host():
+    import torch
+    from synth import device as D
+    for wfmt, H, F in ((S.RVQ, 64, 40), (S.INT4, 256, 128)):
+        host = S.make_expert_blob(5, 2, 3, wfmt, H, F)
+        dev = torch.empty(host.size, dtype=torch.uint8, device="cuda")
+        D.make_expert_blob_device(5, 2, 3, wfmt, H, F, dev)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(dev.cpu().numpy(), host)

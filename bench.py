@@ -1,0 +1,517 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode-time routed MoE layer stack on GB300 (one JSON line).
+
+Default workload: the Mixtral-shaped stack - 32 MoE layers, H = 4096, F = 14336, 8 experts
+per layer, top-2 softmax router, int4 experts (symmetric, group 128, fp16 scales; 90.8 MB
+per expert, 256 experts = 23 GB resident in HBM), decode T = 1, a 512-token sequence of
+x ~ N(0,1) (bf16) fed layer to layer as x += moe(rmsnorm(x)).  One step = one token
+through all 32 layers (router, gate/up, down, combine and the residual RMS norm of every
+layer), replayed from one CUDA graph with the inputs resident in HBM.  The per-token
+expert working set (2 x 32 x 90.8 MB = 5.8 GB) is far larger than the 129 MB L2, so no
+flush is needed between steps.
+
+Other workloads (``--config``): tiny, dsv3 (T = 1, 4 or 32 via --tokens-per-step),
+wide, stream (HBM LRU cache over a pinned host pool).
+
+Reported: tokens/s (value), expert-weight GB/s against the HBM peak, hit %, the dominant
+kernel's roofline (CUDA events around each kernel, recorded inside the timed graph), the
+end-to-end rate through host buffers, SM clocks sampled during the timed region, and the
+fp64 CPU oracle timed on a bounded sample (``cpu_baseline``).  ``--impl reference`` times
+that oracle alone on the same workload.  N > 1 GPUs (torchrun) run independent replicas:
+the layer does not shard (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth as S  # noqa: E402
+
+CONFIGS = {
+    "tiny": dict(workload="tiny MoE layer: 1 layer, H=256, F=512, 8 experts, top-2 softmax, RVQ-3bit, T=4",
+                 layers=1, H=256, F=512, E=8, k=2, router=0, shared=False, wfmt=S.RVQ, T=4,
+                 tokens=64, trace="iid", cache=0),
+    "mixtral": dict(workload="Mixtral-shaped stack: 32 MoE layers, H=4096, F=14336, 8 experts, top-2 softmax, "
+                             "int4 g128 fp16 scales, all 256 experts resident, decode T=1, 512-token sequence",
+                    layers=32, H=4096, F=14336, E=8, k=2, router=0, shared=False, wfmt=S.INT4, T=1,
+                    tokens=512, trace="iid", cache=0),
+    "dsv3": dict(workload="DeepSeek-V3-shaped stack: 58 MoE layers, H=7168, 256 routed experts F=2048 + 1 shared, "
+                          "sigmoid top-8 normalised, RVQ-3bit, all resident",
+                 layers=58, H=7168, F=2048, E=256, k=8, router=1, shared=True, wfmt=S.RVQ, T=1,
+                 tokens=256, trace="iid", cache=0),
+    "wide": dict(workload="Wide top-16 stack: 24 MoE layers, H=7168, 384 experts F=1536, top-16 softmax, RVQ-3bit, "
+                          "all resident, decode T=1 over a 1024-token domain-local trace",
+                 layers=24, H=7168, F=1536, E=384, k=16, router=0, shared=False, wfmt=S.RVQ, T=1,
+                 tokens=1024, trace="domain", cache=0),
+    "stream": dict(workload="Streaming tier: 48 MoE layers x 256 experts, H=7168, F=1536, top-16, RVQ-3bit, pinned "
+                            "host pool, 32 GB HBM LRU cache, side-stream miss copies, 4096-token domain-local trace",
+                   layers=48, H=7168, F=1536, E=256, k=16, router=0, shared=False, wfmt=S.RVQ, T=1,
+                   tokens=4096, trace="domain", cache=32_000_000_000),
+}
+# one-layer cuts of the big shapes (a few GB on the device), for profiler captures
+for _n, _src in (("mixtral1", "mixtral"), ("dsv3-1", "dsv3"), ("wide1", "wide")):
+    CONFIGS[_n] = dict(CONFIGS[_src], layers=1, workload="one layer of the " + CONFIGS[_src]["workload"])
+SEED = 0
+L2_BYTES = 129e6
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------- peaks, clocks
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in mp:
+                return float(mp[key]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (MEASURED_PEAKS.json absent)"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- inputs
+def token_inputs(cfg, n):
+    """[n, T, H] float32 values (bf16-rounded): the workload's token process."""
+    H, T = cfg["H"], cfg["T"]
+    if cfg["trace"] == "domain":
+        x = S.make_domain_trace(SEED, 0, n * T, H)
+    else:
+        x = S.make_tokens(SEED, 0, n * T, H)
+    return x.reshape(n, T, H)
+
+
+def build_context(cfg, device, max_tokens):
+    """Create the context and register every router and expert (blobs made on the GPU)."""
+    import torch
+    import routed_expert_ffn_03_gb300 as M
+    from synth import device as D
+    t0 = time.time()
+    ctx = M.Context(cfg["layers"], cfg["H"], cfg["F"], cfg["E"], cfg["k"], cfg["wfmt"], router=cfg["router"],
+                    shared_ffn=cfg["F"] if cfg["shared"] else 0, max_tokens=max_tokens,
+                    hbm_cache_bytes=cfg["cache"], device=device)
+    nb = S.expert_blob_bytes(cfg["wfmt"], cfg["H"], cfg["F"])
+    blob = torch.empty(nb, dtype=torch.uint8, device="cuda:%d" % device)
+    experts = list(range(cfg["E"])) + ([-1] if cfg["shared"] else [])
+    for l in range(cfg["layers"]):
+        ctx.register_router(l, S.make_router(SEED, l, cfg["E"], cfg["H"]))
+        for e in experts:
+            D.make_expert_blob_device(SEED, l, e, cfg["wfmt"], cfg["H"], cfg["F"], blob,
+                                      stream=torch.cuda.current_stream().cuda_stream)
+            ctx.register_expert(l, e, blob)
+    del blob
+    torch.cuda.synchronize()
+    log("registered %d layers x %d experts in %.1f s" % (cfg["layers"], len(experts), time.time() - t0))
+    return ctx
+
+
+def gateup_bytes_per_expert(cfg):
+    H, F = cfg["H"], cfg["F"]
+    if cfg["wfmt"] == S.INT4:
+        return 2 * (F * H // 2 + F * (H // 128) * 2)
+    return 2 * (3 * 256 * 8 * 2 + F * (H // 8) * 3)
+
+
+def kernel_source_hash(wfmt):
+    name = "int4.cu" if wfmt == S.INT4 else "rvq.cu"
+    with open(os.path.join(ROOT, "routed_expert_ffn_03_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(cfg_name, wfmt):
+    """Per-launch DRAM bytes of the gate/up kernel from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            tab = json.load(f)
+        ent = tab.get(cfg_name)
+        if ent and ent.get("source_sha256_16") == kernel_source_hash(wfmt):
+            return float(ent["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_layer_sample(cfg, n_tokens, n_layers, device):
+    """Time the fp64 oracle stack on tokens 0..n_tokens-1 through layers 0..n_layers-1.
+    Expert blobs are generated on demand; the time spent making them is not counted."""
+    import torch
+    from oracle import oracle as O
+    from synth import device as D
+    x0 = token_inputs(cfg, n_tokens)[:, 0, :] if cfg["T"] == 1 else token_inputs(cfg, 1)[0][:n_tokens]
+    nb = S.expert_blob_bytes(cfg["wfmt"], cfg["H"], cfg["F"])
+    dev = torch.empty(nb, dtype=torch.uint8, device="cuda:%d" % device)
+    cache = {}
+    gen_time = [0.0]
+
+    def blob(l, e):
+        if (l, e) not in cache:
+            t = time.perf_counter()
+            D.make_expert_blob_device(SEED, l, e, cfg["wfmt"], cfg["H"], cfg["F"], dev)
+            cache[(l, e)] = dev.cpu().numpy()
+            gen_time[0] += time.perf_counter() - t
+        return cache[(l, e)]
+
+    routers = [S.make_router(SEED, l, cfg["E"], cfg["H"]) for l in range(n_layers)]
+    layers = []
+    for l in range(n_layers):
+        def fn(xn, l=l):
+            return O.layer(xn, routers[l], cfg["k"], cfg["router"], lambda e: blob(l, e), cfg["wfmt"],
+                           cfg["H"], cfg["F"], blob(l, -1) if cfg["shared"] else None,
+                           cfg["F"] if cfg["shared"] else 0)
+        layers.append(fn)
+    t0 = time.perf_counter()
+    O.stack(x0, layers)
+    dt = time.perf_counter() - t0 - gen_time[0]
+    del dev
+    return dt, O.threads()
+
+
+def cpu_baseline(cfg, device):
+    n_tok, n_lay = (4, min(cfg["layers"], 8)) if cfg["wfmt"] == S.INT4 else (2, min(cfg["layers"], 4))
+    if cfg["name"] == "tiny":
+        n_tok, n_lay = 4, 1
+    dt, cores = oracle_layer_sample(cfg, n_tok, n_lay, device)
+    per_token = dt / n_tok * cfg["layers"] / n_lay
+    return {"value": cfg["T"] / per_token if cfg["T"] > 1 and cfg["name"] == "tiny" else 1.0 / per_token,
+            "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "fp64 oracle (router, top-k, explicit dequant, dense SwiGLU, combine, rmsnorm stack) on "
+                      "%d tokens x the first %d of %d layers, %.1f s, extrapolated to the full stack"
+                      % (n_tok, n_lay, cfg["layers"], dt)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args, cfg, rank, world, device):
+    import torch
+    torch.cuda.set_device(device)
+    import routed_expert_ffn_03_gb300 as M  # noqa: F401
+    T = cfg["T"]
+    ctx = build_context(cfg, device, max_tokens=T)
+    H, L = cfg["H"], cfg["layers"]
+    n_inp = cfg["tokens"]
+    x0_host = torch.from_numpy(np.ascontiguousarray(token_inputs(cfg, n_inp))).float()   # [n, T, H]
+    x0_dev = x0_host.cuda(device)
+    x = torch.zeros((T, H), dtype=torch.float32, device=device)
+    y = torch.zeros((T, H), dtype=torch.float32, device=device)
+    xn = torch.zeros((T, H), dtype=torch.int16, device=device)
+    stream = torch.cuda.Stream(device=device)
+    streamed = cfg["cache"] != 0
+
+    def layers():
+        for l in range(L):
+            ctx.residual_rmsnorm(x, None if l == 0 else y, xn, T)
+            ctx.forward(l, xn, y, T)
+        ctx.residual_rmsnorm(x, y, xn, T)
+
+    graph = None
+    with torch.cuda.stream(stream):
+        x.copy_(x0_dev[0])
+        layers()
+    torch.cuda.synchronize()
+    if not streamed:
+        ctx.profile(True)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            layers()
+        torch.cuda.synchronize()
+
+    def step(i):
+        x.copy_(x0_dev[i % n_inp])
+        if graph is not None:
+            graph.replay()
+        else:
+            layers()
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    torch.cuda.synchronize()
+    ctx.reset_stats()
+    hit_series = []
+    clocks = ClockSampler(device)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(K):
+            step(W + i)
+            if streamed and (i + 1) % 64 == 0:
+                st = ctx.stats()
+                hit_series.append(round(st["hits"] / max(1, st["lookups"]), 4))
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    st = ctx.stats()
+    prof = None
+    if graph is not None:
+        try:
+            prof = ctx.profile_read()
+        except Exception as e:  # noqa: BLE001
+            log("profile_read failed: %s" % e)
+    secs = ms / 1e3
+    tok_s = world * K * T / secs
+    expert_gbs = st["bytes_expert_touched"] / secs / 1e9
+    peak, peak_src = hbm_peak()
+
+    # e2e: same steps through host (pinned) buffers, copies inside the timed region
+    e2e = None
+    if graph is not None:
+        xh = x0_host.pin_memory()
+        outh = torch.empty((min(K, 64), T, H), dtype=torch.float32).pin_memory()
+        with torch.cuda.stream(stream):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(K):
+                x.copy_(xh[(W + i) % n_inp], non_blocking=True)
+                graph.replay()
+                outh[i % outh.shape[0]].copy_(x, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        e2e = {"value": round(world * K * T / (ems / 1e3), 3), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * H * 4, "d2h_bytes_per_step": T * H * 4}
+
+    roofline = None
+    if prof is not None:
+        ms4, nl = prof
+        if nl > 0:
+            uniq_per_layer = st["lookups"] / max(1, st["forwards"])
+            experts_per_launch = uniq_per_layer + (1 if cfg["shared"] else 0)
+            alg = experts_per_launch * gateup_bytes_per_expert(cfg)
+            dur = ms4[1] / nl / 1e3
+            ach = alg / dur / 1e9
+            tr = ncu_traffic(cfg["name"], cfg["wfmt"])
+            roofline = {"bound": "hbm", "kernel": "int4_kernel<gate/up>" if cfg["wfmt"] == S.INT4 else "rvq_kernel<gate/up>",
+                        "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                        "traffic": tr, "peak_source": peak_src,
+                        "alg_bytes_per_launch": int(alg), "avg_launch_us": round(dur * 1e6, 2),
+                        "per_kernel_us": {n: round(v / nl * 1e3, 2) for n, v in
+                                          zip(("router", "gateup", "down", "combine"), ms4)}}
+    out = {
+        "metric": "MoE decode tokens/s; expert-weight GB/s vs HBM peak; cache hit % (1 GB300)",
+        "value": round(tok_s, 3), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 x fp16(hi+lo) -> fp32" if cfg["wfmt"] == S.INT4 else "rvq3 (fp16 codebooks) x fp32 LUT -> fp32",
+        "data": "synthetic (seeded SplitMix64 weights and inputs, no trained weights)",
+        "config": {"workload": cfg["workload"], "layers": L, "hidden": H, "ffn": cfg["F"], "experts": cfg["E"],
+                   "top_k": cfg["k"], "tokens_per_step": T, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "graph": graph is not None,
+                   "l2": "no flush: per-step expert working set %.2f GB > 129 MB L2" % (
+                       st["bytes_expert_touched"] / max(1, K) / 1e9)},
+        "expert_gbs": round(expert_gbs, 1), "hbm_frac": round(expert_gbs / peak, 4),
+        "hit_rate": round(st["hits"] / max(1, st["lookups"]), 4),
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": K * (L * 5 + 1),
+        "clocks": clk,
+        "wall_s": round(wall, 3),
+    }
+    if streamed:
+        out["hit_series_per64"] = hit_series
+        out["h2d_gbs"] = round(st["bytes_h2d"] / max(1e-9, st["h2d_ms"] / 1e3) / 1e9, 2) if st["h2d_ms"] else None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ctx.close()
+        torch.cuda.empty_cache()
+        out["cpu_baseline"] = cpu_baseline(cfg, device)
+    else:
+        ctx.close()
+    return out
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, cfg, device):
+    """The fp64 oracle alone: each step = one token's router + one matrix of one selected
+    expert of one layer (layers cycle over the first few), so the whole run stays within
+    minutes; the rate is extrapolated to the full stack."""
+    from oracle import oracle as O
+    import torch
+    from synth import device as D
+    nl = min(cfg["layers"], 2)
+    xin = token_inputs(cfg, max(1, min(cfg["tokens"], 64)))
+    routers = [S.make_router(SEED, l, cfg["E"], cfg["H"]) for l in range(nl)]
+    nb = S.expert_blob_bytes(cfg["wfmt"], cfg["H"], cfg["F"])
+    dev = torch.empty(nb, dtype=torch.uint8, device="cuda:%d" % device) if torch.cuda.is_available() else None
+    cache = {}
+
+    def blob(l, e):
+        if (l, e) not in cache:
+            if dev is not None:
+                D.make_expert_blob_device(SEED, l, e, cfg["wfmt"], cfg["H"], cfg["F"], dev)
+                cache[(l, e)] = dev.cpu().numpy()
+            else:
+                cache[(l, e)] = S.make_expert_blob(SEED, l, e, cfg["wfmt"], cfg["H"], cfg["F"])
+        return cache[(l, e)]
+
+    shapes = S.matrix_shapes(cfg["H"], cfg["F"])
+    offs = np.cumsum([0] + [S.matrix_block_bytes(cfg["wfmt"], r, kk) for r, kk in shapes])
+    t_router, t_mat = [], [[], [], []]
+    for i in range(args.warmup + args.steps):
+        l = i % nl
+        m = i % 3                      # gate, up, down in rotation
+        xb = O.rmsnorm_bf16(xin[i % xin.shape[0]])
+        t0 = time.perf_counter()
+        r = O.router(xb, routers[l], cfg["k"], cfg["router"])
+        t1 = time.perf_counter()
+        e = int(r["idx"][0, (i // 3) % cfg["k"]])
+        b = blob(l, e)
+        rows, K = shapes[m]
+        xv = O.bf16_value(xb[:1])
+        if K != xv.shape[1]:            # down input: the token's values tiled to F (timing only)
+            xv = np.resize(xv, (1, K))
+        t2 = time.perf_counter()
+        O.matvec(cfg["wfmt"], rows, K, b[offs[m]:offs[m + 1]], xv)
+        t3 = time.perf_counter()
+        if i >= args.warmup:
+            t_router.append(t1 - t0)
+            t_mat[m].append(t3 - t2)
+    t_expert = [sum(statistics.mean(v) for v in t_mat if v)]
+    per_layer_token = statistics.mean(t_router) + (cfg["k"] + (1 if cfg["shared"] else 0)) * statistics.mean(t_expert)
+    value = cfg["T"] / (per_layer_token * cfg["T"] * cfg["layers"])
+    return {
+        "impl": "reference",
+        "metric": "MoE decode tokens/s; expert-weight GB/s vs HBM peak; cache hit % (1 GB300)",
+        "value": round(value, 6), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * (statistics.mean(t_router) + t_expert[0] / 3), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64 weights and inputs)",
+        "config": {"workload": cfg["workload"], "layers": cfg["layers"], "hidden": cfg["H"], "ffn": cfg["F"],
+                   "experts": cfg["E"], "top_k": cfg["k"], "tokens_per_step": cfg["T"]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "tokens/s", "cores": O.threads(), "kind": "oracle",
+                         "sample": "each step: fp64 oracle router + one matrix (gate, up, down in rotation) of one "
+                                   "selected expert for one token at layer (step mod %d); tokens/s = 1 / (layers x "
+                                   "(router + k x (gate + up + down)))" % nl},
+        "e2e": {"value": round(value, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral", choices=sorted(CONFIGS))
+    ap.add_argument("--tokens-per-step", type=int, default=0, help="override T (dsv3: 1, 4, 32)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    cfg = dict(CONFIGS[args.config])
+    cfg["name"] = args.config
+    if args.tokens_per_step:
+        cfg["T"] = args.tokens_per_step
+        cfg["workload"] += " (T=%d per step)" % cfg["T"]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import __graft_entry__ as G
+        G.build()
+        print(json.dumps(run_reference(args, cfg, local)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        import __graft_entry__ as G
+        G.build()
+    if world > 1:
+        torch.distributed.barrier()
+    out = run_gpu(args, cfg, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -269,9 +269,9 @@ def run_gpu(args, cfg, rank, world, device):
     streamed = cfg["cache"] != 0
 
     def layers():
+        # x += y_prev; xn = rmsnorm(x); y = layer(xn)   (fused stack step), then the last add
         for l in range(L):
-            ctx.residual_rmsnorm(x, None if l == 0 else y, xn, T)
-            ctx.forward(l, xn, y, T)
+            ctx.forward_residual(l, x, None if l == 0 else y, xn, y, T)
         ctx.residual_rmsnorm(x, y, xn, T)
 
     graph = None
@@ -280,7 +280,6 @@ def run_gpu(args, cfg, rank, world, device):
         layers()
     torch.cuda.synchronize()
     if not streamed:
-        ctx.profile(True)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             layers()
@@ -325,12 +324,6 @@ def run_gpu(args, cfg, rank, world, device):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     st = ctx.stats()
-    prof = None
-    if graph is not None:
-        try:
-            prof = ctx.profile_read()
-        except Exception as e:  # noqa: BLE001
-            log("profile_read failed: %s" % e)
     secs = ms / 1e3
     tok_s = world * K * T / secs
     expert_gbs = st["bytes_expert_touched"] / secs / 1e9
@@ -355,6 +348,27 @@ def run_gpu(args, cfg, rank, world, device):
         e2e = {"value": round(world * K * T / (ems / 1e3), 3), "unit": "tokens/s",
                "h2d_bytes_per_step": T * H * 4, "d2h_bytes_per_step": T * H * 4}
 
+    # per-kernel durations: CUDA events around every kernel (event nodes of a second graph
+    # of the same step, replayed on the same stream); kept out of the headline timing above
+    prof = None
+    if graph is not None:
+        try:
+            ctx.profile(True)
+            pgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(pgraph, stream=stream):
+                layers()
+            acc4, nacc = [0.0] * 4, 0
+            with torch.cuda.stream(stream):
+                for i in range(args.prof_steps):
+                    x.copy_(x0_dev[(W + K + i) % n_inp])
+                    pgraph.replay()
+                    ms4_i, nl_i = ctx.profile_read()
+                    acc4 = [u + v for u, v in zip(acc4, ms4_i)]
+                    nacc += nl_i
+            ctx.profile(False)
+            prof = (acc4, nacc)
+        except Exception as e:  # noqa: BLE001
+            log("per-kernel profile failed: %s" % e)
     roofline = None
     if prof is not None:
         ms4, nl = prof
@@ -365,10 +379,12 @@ def run_gpu(args, cfg, rank, world, device):
             dur = ms4[1] / nl / 1e3
             ach = alg / dur / 1e9
             tr = ncu_traffic(cfg["name"], cfg["wfmt"])
-            roofline = {"bound": "hbm", "kernel": "int4_kernel<gate/up>" if cfg["wfmt"] == S.INT4 else "rvq_kernel<gate/up>",
+            roofline = {"bound": "hbm", "kernel": "int4_gateup_kernel" if cfg["wfmt"] == S.INT4 else "rvq_kernel<gate/up>",
                         "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
                         "traffic": tr, "peak_source": peak_src,
                         "alg_bytes_per_launch": int(alg), "avg_launch_us": round(dur * 1e6, 2),
+                        "timing": "CUDA events around each kernel on its stream, %d replays x %d layers "
+                                  "(event nodes in a separate copy of the step graph)" % (args.prof_steps, cfg["layers"]),
                         "per_kernel_us": {n: round(v / nl * 1e3, 2) for n, v in
                                           zip(("router", "gateup", "down", "combine"), ms4)}}
     out = {
@@ -385,7 +401,7 @@ def run_gpu(args, cfg, rank, world, device):
         "expert_gbs": round(expert_gbs, 1), "hbm_frac": round(expert_gbs / peak, 4),
         "hit_rate": round(st["hits"] / max(1, st["lookups"]), 4),
         "roofline": roofline, "e2e": e2e,
-        "gpu_launches": K * (L * 5 + 1),
+        "gpu_launches": K * (L * 4 + 1),
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
@@ -476,6 +492,7 @@ def main():
     ap.add_argument("--config", default="mixtral", choices=sorted(CONFIGS))
     ap.add_argument("--tokens-per-step", type=int, default=0, help="override T (dsv3: 1, 4, 32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prof-steps", type=int, default=16, help="replays of the per-kernel event graph")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -146,6 +146,15 @@ size_t moe_expert_blob_bytes(int wfmt, int hidden, int ffn);
  * range, null pointers), MOE_ESTATE (layer not fully registered), sticky errors. */
 moe_status moe_forward(moe_ctx* ctx, int layer, const void* x_bf16, float* out, int T, void* stream);
 
+/* One layer of the residual stack, fused:  if y_prev != NULL: x += y_prev;
+ * xn = bf16(x / sqrt(mean(x^2) + eps));  y = layer(xn)  (as moe_forward).
+ * x fp32 [T,H] in/out, y_prev fp32 [T,H] or NULL (it may be the same buffer as y),
+ * xn bf16 bits [T,H] out, y fp32 [T,H] out; all device pointers.  Same bits as
+ * moe_residual_rmsnorm followed by moe_forward; for small T the norm runs inside the
+ * router kernel instead of a kernel of its own. */
+moe_status moe_forward_residual(moe_ctx* ctx, int layer, float* x, const float* y_prev, uint16_t* xn,
+                                float* y, int T, float eps, void* stream);
+
 /* The routing of the last forward of `layer`: idx[T][k] (int32, descending score) and
  * w[T][k] (fp32) into host buffers; *T_out = that forward's T.  Synchronises the device.
  * MOE_ENOTFOUND before the first forward of the layer. */
@@ -167,6 +176,17 @@ moe_status moe_reset_stats(moe_ctx* ctx);
 moe_status moe_destroy(moe_ctx* ctx);
 
 const char* moe_strerror(moe_status s);
+
+/* ---- measurement (no counterpart in the pages) ---- */
+
+/* Per-kernel timing: when enabled, moe_forward records CUDA events (timing enabled) on its
+ * stream before the router and after the router, gate/up, down and combine kernels of
+ * each layer (inside a CUDA graph capture they become event nodes of the graph).
+ * moe_profile_read synchronises the device and returns, summed over the layers whose
+ * latest forward was recorded, the milliseconds of [router, gate/up, down, combine] in
+ * ms[0..3], and that number of layers in *n_layers.  Resident mode only. */
+moe_status moe_profile(moe_ctx* ctx, int enable);
+moe_status moe_profile_read(moe_ctx* ctx, double* ms, int* n_layers);
 
 /* ---- test hooks (no counterpart in the pages; failure injection on the host) ---- */
 

@@ -3,83 +3,105 @@
 //
 // Combine: out[t][r] = sum_{j = 0..k-1} w[t][j] * y_{t,j}[r]  (+ y_shared[t][r]),
 // in rank order j, the shared expert (weight 1) added last; y of one pass is the sum of
-// its down-projection k-slice partials in slice order.  The order never depends on
-// timing, so the result is the same bits whatever the cache did.
+// its down-projection k-slice partials (part_d[pass][ks][slot][row]) in a fixed order.
+// The order never depends on timing, so the result is the same bits whatever the cache
+// did.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
-__global__ void combine_kernel(CombineArgs a) {
+// Block = 32 output rows x 8 k-slice lanes.  Lane kl sums slices kl, kl+8, ... of each
+// selected expert in slice order; the 8 lane sums are then added in lane order, the
+// experts in rank order, the shared expert last.
+constexpr int CB_ROWS = 32, CB_KL = 8, CB_MAXJ = 33;
+__global__ void __launch_bounds__(CB_ROWS * CB_KL) combine_kernel(CombineArgs a) {
+  __shared__ float red[CB_KL][CB_MAXJ][CB_ROWS];
+  pdl_wait();  // part_d and the plan come from the kernels before
+  pdl_launch_dependents();
   const int t = blockIdx.y;
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= a.H) return;
+  const int rl = threadIdx.x & (CB_ROWS - 1), kl = threadIdx.x / CB_ROWS;
+  const int r = blockIdx.x * CB_ROWS + rl;
   const int rows32 = cdiv(a.H, 32) * 32;
-  const size_t ks_stride = (size_t)rows32 * a.pmax;
-  float acc = 0.f;
-  for (int j = 0; j < a.k; ++j) {
-    const int pass = a.plan.pair_pass[t * a.k + j];
-    const int slot = a.plan.pair_slot[t * a.k + j];
-    const float* src = a.part_d + (size_t)pass * a.nks_d * ks_stride + (size_t)r * a.pmax + slot;
-    float y = 0.f;
-    for (int ks = 0; ks < a.nks_d; ++ks) y += __ldcg(src + ks * ks_stride);
-    acc = fmaf(a.plan.w[t * a.k + j], y, acc);
+  const size_t slot_stride = rows32, ks_stride = (size_t)a.pmax * rows32;
+  const int nj = a.k + (a.has_shared ? 1 : 0);
+  for (int j = 0; j < nj; ++j) {
+    int pass, slot;
+    if (j < a.k) {
+      pass = a.plan.pair_pass[t * a.k + j];
+      slot = a.plan.pair_slot[t * a.k + j];
+    } else {
+      pass = a.plan.shared_pass[t];
+      slot = a.plan.shared_slot[t];
+    }
+    float s = 0.f;
+    if (r < a.H) {
+      const float* src = a.part_d + (size_t)pass * a.nks_d * ks_stride + slot * slot_stride + r;
+      for (int k0 = kl; k0 < a.nks_d; k0 += 8 * CB_KL) {  // 8 loads in flight, added in order
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int ks = k0 + q * CB_KL;
+          v[q] = ks < a.nks_d ? __ldcg(src + ks * ks_stride) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s += v[q];
+      }
+    }
+    red[kl][j][rl] = s;
   }
-  if (a.has_shared) {
-    const int pass = a.plan.shared_pass[t];
-    const int slot = a.plan.shared_slot[t];
-    const float* src = a.part_d + (size_t)pass * a.nks_d * ks_stride + (size_t)r * a.pmax + slot;
-    float y = 0.f;
-    for (int ks = 0; ks < a.nks_d; ++ks) y += __ldcg(src + ks * ks_stride);
-    acc += y;
+  __syncthreads();
+  if (kl == 0 && r < a.H) {
+    float acc = 0.f;
+    for (int j = 0; j < nj; ++j) {
+      float y = 0.f;
+#pragma unroll
+      for (int q = 0; q < CB_KL; ++q) y += red[q][j][rl];
+      if (j < a.k) acc = fmaf(a.plan.w[t * a.k + j], y, acc);
+      else acc += y;
+    }
+    a.out[(size_t)t * a.H + r] = acc;
   }
-  a.out[(size_t)t * a.H + r] = acc;
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
-  dim3 grid(cdiv(a.H, 256), a.T);
-  combine_kernel<<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cdiv(a.H, CB_ROWS), a.T);
+  cfg.blockDim = dim3(CB_ROWS * CB_KL);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
-// x += y (y may be null); xn = bf16(x / sqrt(mean(x^2) + eps)).  One block per row; the
-// sum of squares is reduced in a fixed order.
-__global__ void residual_rmsnorm_kernel(float* __restrict__ x, const float* __restrict__ y,
-                                        uint16_t* __restrict__ xn, int H, float eps) {
+// x += y (y may be null); xn = bf16(x / sqrt(mean(x^2) + eps)).  One block of 256
+// threads per row; the sum of squares is reduced in the fixed order of block_inv_rms, the
+// same one the router's fused stack step uses.
+__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(float* __restrict__ x, const float* __restrict__ y,
+                                                               uint16_t* __restrict__ xn, int H, float eps) {
   __shared__ float red[32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   float* xr = x + (size_t)t * H;
-  float ss = 0.f;
+  const float* yr = y ? y + (size_t)t * H : nullptr;
+  const float inv = block_inv_rms(xr, yr, H, eps, red);
   for (int h = threadIdx.x; h < H; h += blockDim.x) {
     float v = xr[h];
-    if (y) {
-      v += y[(size_t)t * H + h];
+    if (yr) {
+      v += yr[h];
       xr[h] = v;
     }
-    ss = fmaf(v, v, ss);
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (threadIdx.x == 0) red[0] = v;
-  }
-  __syncthreads();
-  const float inv = rsqrtf(red[0] / (float)H + eps);
-  for (int h = threadIdx.x; h < H; h += blockDim.x) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(xr[h] * inv);
-    xn[(size_t)t * H + h] = __bfloat16_as_ushort(b);
+    xn[(size_t)t * H + h] = __bfloat16_as_ushort(__float2bfloat16_rn(v * inv));
   }
 }
 
 cudaError_t launch_residual_rmsnorm(float* x, const float* y, uint16_t* xn, int T, int H, float eps,
                                     cudaStream_t s) {
-  residual_rmsnorm_kernel<<<T, 256, 0, s>>>(x, y, xn, H, eps);
-  return cudaGetLastError();
+  return launch_pdl(residual_rmsnorm_kernel, T, 256, 0, s, x, y, xn, H, eps);
 }
 
 // One bounded wait on an mbarrier phase that nothing completes.  On expiry it records

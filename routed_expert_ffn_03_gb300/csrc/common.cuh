@@ -129,3 +129,46 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 }
 
 }  // namespace moe
+
+namespace moe {
+// ---------------------------------------------------------------- programmatic dependent launch
+// wait: block until the preceding kernel in the stream has completed and its memory is
+// visible (a no-op when the launch did not ask for programmatic serialisation).
+// launch_dependents: let the next kernel's blocks be scheduled now; they still run their
+// own wait before reading what this kernel writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+}  // namespace moe
+
+namespace moe {
+// 1 / sqrt(mean((x + y)^2) + eps) over one row of H values (y may be null), reduced in a
+// fixed order (thread-strided partial sums, then warp and block trees), so every block
+// that calls it on the same row gets the same bits.  All threads of the block call it;
+// red needs 32 floats.
+__device__ __forceinline__ float block_inv_rms(const float* x, const float* y, int H, float eps, float* red) {
+  float ss = 0.f;
+#pragma unroll 4
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    float v = __ldcg(x + h);
+    if (y) v += __ldcg(y + h);
+    ss = fmaf(v, v, ss);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / (float)H + eps);
+  __syncthreads();
+  return inv;
+}
+}  // namespace moe

@@ -33,11 +33,6 @@
 #include "common.cuh"
 #include "kernels.h"
 
-namespace moe {
-cudaError_t int4_set_attributes();
-cudaError_t rvq_set_attributes();
-}  // namespace moe
-
 using namespace moe;
 
 namespace {
@@ -114,7 +109,8 @@ struct moe_ctx {
   int* d_store_idx = nullptr;
   float* d_store_w = nullptr;
   std::vector<int> last_T;
-  float* d_part_gu = nullptr;
+  float* d_part_gu = nullptr;  // RVQ gate/up k-slice partials
+  float* d_h = nullptr;        // int4 SwiGLU outputs
   float* d_part_d = nullptr;
   int max_pass = 0;
   uint32_t* d_status = nullptr;
@@ -132,6 +128,10 @@ struct moe_ctx {
   int fail_copies = 0;
   moe_status sticky = MOE_OK;
   unsigned long long budget = kDefaultBudget;
+
+  bool prof = false;
+  std::vector<cudaEvent_t> prof_ev;  // [L][5]
+  std::vector<char> prof_seen;       // [L]
 };
 
 namespace {
@@ -187,12 +187,14 @@ void free_all(moe_ctx* c) {
   cudaFree(c->d_store_idx);
   cudaFree(c->d_store_w);
   cudaFree(c->d_part_gu);
+  cudaFree(c->d_h);
   cudaFree(c->d_part_d);
   cudaFree(c->d_status);
   cudaFree(c->d_dbg_status);
   cudaFree(c->d_counters);
   if (c->h_rb) cudaFreeHost(c->h_rb);
   for (auto ev : c->copy_ev) cudaEventDestroy(ev);
+  for (auto ev : c->prof_ev) cudaEventDestroy(ev);
   if (c->side) cudaStreamDestroy(c->side);
   if (c->reg) cudaStreamDestroy(c->reg);
   cudaFree(c->d_blob_stage);
@@ -212,6 +214,7 @@ moe_status validate(const moe_config* g) {
     if (g->hidden % 8 || g->ffn % 8) return MOE_EINVAL;
   } else if (g->wfmt == MOE_W_INT4_G128) {
     if (g->hidden % 128 || g->ffn % 128) return MOE_EINVAL;
+    if (g->hidden > 8192) return MOE_EINVAL;  // the gate/up kernel stages all of x
   } else {
     return MOE_EINVAL;
   }
@@ -278,9 +281,15 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
 
   // scratch geometry
   c->max_pass = maxT * k + (c->has_shared ? maxT : 0);
+  if (cdiv(c->max_pass, c->num_sms) + 2 > 512) {  // passes one expert-kernel block may touch
+    delete c;
+    return MOE_EINVAL;
+  }
   const MatGeom& gg = c->rg.m[0];
   const MatGeom& gd = c->rg.m[2];
+  const bool int4 = cfg->wfmt == MOE_W_INT4_G128;
   const size_t part_gu = (size_t)c->max_pass * 2 * gg.nks * gg.ntask * 32 * c->pmax;
+  const size_t hbuf = int4 ? (size_t)c->max_pass * c->pmax * gg.ntask * 32 : 0;
   const size_t part_d = (size_t)c->max_pass * gd.nks * gd.ntask * 32 * c->pmax;
   const size_t rpart = (size_t)E * router_nch(H) * maxT;
   const size_t router_bytes = (size_t)L * E * H * sizeof(float);
@@ -309,7 +318,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     delete c;
     return MOE_ECUDA;
   }
-  const size_t need = expert_bytes + router_bytes + (part_gu + part_d + rpart) * 4 +
+  const size_t need = expert_bytes + router_bytes + (part_gu + hbuf + part_d + rpart) * 4 +
                       2 * c->blob_bytes + (64ull << 20);
   if (need + (1ull << 30) > free_b) {
     delete c;
@@ -368,7 +377,8 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   AL(c->d_router, router_bytes);
   AL(c->d_rpart, rpart * sizeof(float));
   AL(c->d_ticket, sizeof(unsigned int));
-  AL(c->d_part_gu, part_gu * sizeof(float));
+  if (part_gu) AL(c->d_part_gu, part_gu * sizeof(float));
+  if (hbuf) AL(c->d_h, hbuf * sizeof(float));
   AL(c->d_part_d, part_d * sizeof(float));
   AL(c->d_status, 4);
   AL(c->d_dbg_status, 4);
@@ -403,7 +413,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   cudaMemset(c->d_plan_mem, 0, 16 * sizeof(int));
   if (cudaStreamCreateWithFlags(&c->reg, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
-      router_set_attributes() != cudaSuccess || int4_set_attributes() != cudaSuccess ||
+      router_set_attributes() != cudaSuccess || int4_set_attributes(H, maxT) != cudaSuccess ||
       rvq_set_attributes() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     free_all(c);
@@ -490,6 +500,8 @@ static ExpertArgs expert_args(moe_ctx* c, uint8_t* const* table, const void* x, 
   a.T = T;
   a.x = (const uint16_t*)x;
   a.part_gu = c->d_part_gu;
+  a.h = c->d_h;
+  a.max_tokens = c->cfg.max_tokens;
   a.part_d = c->d_part_d;
   a.range.order = nullptr;
   a.range.p_begin = 0;
@@ -546,19 +558,21 @@ static int cache_get(moe_ctx* c, long long key, bool* hit) {
   return s;
 }
 
-moe_status moe_forward(moe_ctx* c, int layer, const void* x, float* out, int T, void* stream) {
-  if (!c || !x || !out || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
-  if (T < 1 || T > c->cfg.max_tokens) return MOE_EINVAL;
-  if (c->sticky != MOE_OK) return c->sticky;
-  moe_status rs = layer_ready(c, layer);
-  if (rs != MOE_OK) return rs;
-  DeviceGuard dg(c->device);
-  cudaStream_t s = (cudaStream_t)stream;
+// Router input: xn (bf16) when xres is null; else the fused stack step on the residual
+// xres (+ yprev), which writes xres and xn_out.
+static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres, const float* yprev,
+                               uint16_t* xn_out, float eps, float* out, int T, cudaStream_t s) {
   const int L = c->cfg.num_layers, E = c->cfg.num_experts, H = c->cfg.hidden, k = c->cfg.top_k;
   (void)L;
 
   RouterArgs ra{};
   ra.x = (const uint16_t*)x;
+  ra.xres = xres;
+  ra.yprev = yprev;
+  ra.xres_out = xres;
+  ra.xn_out = xn_out;
+  ra.eps = eps;
+  if (xres) x = xn_out;  // the expert kernels read the normalised input
   ra.W = c->d_router + (size_t)layer * E * H;
   ra.T = T;
   ra.H = H;
@@ -574,6 +588,7 @@ moe_status moe_forward(moe_ctx* c, int layer, const void* x, float* out, int T, 
   ra.store_w = c->d_store_w + (size_t)layer * c->cfg.max_tokens * k;
   ra.counters = c->d_counters;
   ra.record_bytes = c->rec_bytes;
+  if (c->prof && !c->streamed) CK(cudaEventRecordWithFlags(c->prof_ev[(size_t)layer * 5], s, cudaEventRecordExternal));
   CK(launch_router(ra, c->num_sms, s));
 
   CombineArgs ca{};
@@ -589,8 +604,23 @@ moe_status moe_forward(moe_ctx* c, int layer, const void* x, float* out, int T, 
 
   if (!c->streamed) {
     ExpertArgs a = expert_args(c, c->d_rec_table + (size_t)layer * (E + 1), x, T);
-    CK(launch_experts(c, a, s));
+    cudaEvent_t* ev = c->prof ? &c->prof_ev[(size_t)layer * 5] : nullptr;
+    if (ev) CK(cudaEventRecordWithFlags(ev[1], s, cudaEventRecordExternal));
+    if (c->cfg.wfmt == MOE_W_INT4_G128) {
+      CK(launch_int4_gateup(a, c->num_sms, s));
+      if (ev) CK(cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal));
+      CK(launch_int4_down(a, c->num_sms, s));
+    } else {
+      CK(launch_rvq_gateup(a, c->num_sms, s));
+      if (ev) CK(cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal));
+      CK(launch_rvq_down(a, c->num_sms, s));
+    }
+    if (ev) CK(cudaEventRecordWithFlags(ev[3], s, cudaEventRecordExternal));
     CK(launch_combine(ca, s));
+    if (ev) {
+      CK(cudaEventRecordWithFlags(ev[4], s, cudaEventRecordExternal));
+      c->prof_seen[layer] = 1;
+    }
     c->last_T[layer] = T;
     return MOE_OK;
   }
@@ -701,6 +731,32 @@ moe_status moe_forward(moe_ctx* c, int layer, const void* x, float* out, int T, 
   return MOE_OK;
 }
 
+moe_status moe_forward(moe_ctx* c, int layer, const void* x, float* out, int T, void* stream) {
+  if (!c || !x || !out || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
+  if (T < 1 || T > c->cfg.max_tokens) return MOE_EINVAL;
+  if (c->sticky != MOE_OK) return c->sticky;
+  moe_status rs = layer_ready(c, layer);
+  if (rs != MOE_OK) return rs;
+  DeviceGuard dg(c->device);
+  return forward_impl(c, layer, x, nullptr, nullptr, nullptr, 0.f, out, T, (cudaStream_t)stream);
+}
+
+moe_status moe_forward_residual(moe_ctx* c, int layer, float* x, const float* y_prev, uint16_t* xn, float* y,
+                                int T, float eps, void* stream) {
+  if (!c || !x || !xn || !y || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
+  if (T < 1 || T > c->cfg.max_tokens) return MOE_EINVAL;
+  if (c->sticky != MOE_OK) return c->sticky;
+  moe_status rs = layer_ready(c, layer);
+  if (rs != MOE_OK) return rs;
+  DeviceGuard dg(c->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  // every router block re-reads the T rows to take their norms: fuse only small steps
+  if ((size_t)T * c->cfg.hidden <= 32768 && T <= ROUTER_FUSED_MAXT)
+    return forward_impl(c, layer, nullptr, x, y_prev, xn, eps, y, T, s);
+  CK(launch_residual_rmsnorm(x, y_prev, xn, T, c->cfg.hidden, eps, s));
+  return forward_impl(c, layer, xn, nullptr, nullptr, nullptr, 0.f, y, T, s);
+}
+
 moe_status moe_get_routing(moe_ctx* c, int layer, int* idx, float* w, int* T_out) {
   if (!c || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
   DeviceGuard dg(c->device);
@@ -754,6 +810,43 @@ moe_status moe_reset_stats(moe_ctx* c) {
   CK(cudaMemset(c->d_counters, 0, sizeof(DevCounters)));
   c->hits = c->misses = c->bytes_h2d = 0;
   c->h2d_ms = 0.0;
+  return MOE_OK;
+}
+
+moe_status moe_profile(moe_ctx* c, int enable) {
+  if (!c) return MOE_EINVAL;
+  if (c->streamed && enable) return MOE_EINVAL;
+  DeviceGuard dg(c->device);
+  if (enable && c->prof_ev.empty()) {
+    c->prof_ev.resize((size_t)c->cfg.num_layers * 5);
+    for (auto& ev : c->prof_ev) CK(cudaEventCreate(&ev));
+  }
+  c->prof_seen.assign(c->cfg.num_layers, 0);
+  c->prof = enable != 0;
+  return MOE_OK;
+}
+
+moe_status moe_profile_read(moe_ctx* c, double* ms, int* n_layers) {
+  if (!c || !ms || !n_layers) return MOE_EINVAL;
+  DeviceGuard dg(c->device);
+  moe_status st = check_device(c);
+  if (st != MOE_OK) return st;
+  for (int i = 0; i < 4; ++i) ms[i] = 0.0;
+  int n = 0;
+  for (int l = 0; l < c->cfg.num_layers && !c->prof_ev.empty(); ++l) {
+    if (!c->prof_seen[l]) continue;
+    for (int i = 0; i < 4; ++i) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, c->prof_ev[(size_t)l * 5 + i], c->prof_ev[(size_t)l * 5 + i + 1]) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ENOTFOUND;
+      }
+      ms[i] += t;
+    }
+    ++n;
+  }
+  *n_layers = n;
   return MOE_OK;
 }
 

@@ -1,34 +1,54 @@
-// int4.cu - int4 (symmetric, group 128, fp16 scales) expert GEMV kernels.
+// int4.cu - int4 (symmetric, group 128, fp16 scales) expert kernels.
 //
-// gate/up:  part_gu[pass][m][ks][row][slot] = sum over k in slice ks of W_m[row][k] x[k]
-// down:     part_d [pass][ks][row][slot]    = sum over k in slice ks of W_d[row][k] h[k],
-//           h = silu(g) * u with g, u the slice sums of part_gu added in slice order.
-// A "pass" is one expert with up to 4 tokens; every pass of every selected expert is
-// spread over all SMs as equal contiguous ranges of 32-row x 512-input tasks.
+// gate/up:  part_gu[pass][m][ks][slot][row] = sum over k in slice ks of W_m[row][k] x[k]
+// down:     part_d[pass][ks][slot][row] = sum over k in slice ks of W_d[row][k] h[k],
+//           h = silu(g) * u with g, u the gate / up partials added in k-slice order
+//           (computed by the down kernel for the slice it works on).
+// A "pass" is one expert with up to 4 tokens (slots).
 //
-// Data movement: one producer warp per block streams each task (32 rows x 4 groups =
-// 8448 B, contiguous in the kernel layout) with a 1-D bulk TMA copy into a per-warp
-// ring of shared-memory stages; consumer warps read their stage with conflict-free
-// 16-byte loads.  Arithmetic: a lane dequantises its own m16n8k16 A fragment from 8
-// nibbles (q + 1032 is built as an fp16 bit pattern and the offset removed exactly),
+// Data movement: each of the 16 warps of a block streams its own tasks (32 rows x 2
+// groups of 128 inputs = 4224 B, contiguous in the kernel layout) with 1-D bulk TMA
+// copies into its own ring of shared-memory slots, D tasks ahead of the one it computes,
+// and reads a slot with conflict-free 16-byte loads.
+//
+// Arithmetic: a lane dequantises its own m16n8k16 A fragment from 8 nibbles (q + 1032
+// is built as an fp16 bit pattern with one LOP3 per pair and the offset removed exactly),
 // and the warp-level tensor-core mma multiplies it by the activations, split into fp16
 // hi + lo parts so that hi + lo reproduces fp32 inputs to 2^-22; products of q and an
 // fp16 part are exact and accumulate in fp32.  The fp16 group scale multiplies each
-// 128-wide group's fp32 sum.  The 8 mma columns carry (token, hi/lo) pairs, so one
-// pass serves up to 4 tokens at the cost of one.
+// 128-wide group's fp32 sum.  (Feeding q + 1032 itself and removing 1032 * sum(x) after
+// the mma saves the fp16 subtractions but loses three orders of magnitude of accuracy
+// to the fp32 accumulation of the large offsets, so it is not done.)  The 8 mma columns
+// carry (token, hi/lo) pairs, so one pass serves up to 4 tokens at the cost of one.
+//
+// Work split (both kernels): tasks in a fixed order, blocks take equal contiguous ranges,
+// and a block deals its range to its warps round-robin (task i -> warp (i - t0) mod NW);
+// each warp walks its tasks with incremental counters.  gate/up tasks run in (pass,
+// row block, matrix, k-slice) order; down tasks in (pass, k-slice, row block) order and
+// leave k-slice partials for the combine kernel.  The B fragments are kept only for the
+// mma columns that carry tokens (2 per token), which leaves room for 3 ring slots per
+// warp when a pass has one token.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
-constexpr int I4_NW = 8;                                // consumer warps
-constexpr int I4_D = 2;                                 // ring stages per consumer warp
-constexpr int I4_STAGE = I4_KS * I4_PAIR_BLOCK;         // 8448 B
-constexpr int I4_KSTEPS = I4_KS * I4_GROUP / 16;        // 32 mma k-steps per slice
-constexpr int I4_XFRAG = I4_KSTEPS * 32 * 8;            // 8192 B of B fragments
-constexpr int I4_VIN = I4_PMAX * I4_KS * I4_GROUP * 4;  // 8192 B of slice inputs
-constexpr int I4_BAR_OFF = I4_NW * I4_D * I4_STAGE + I4_XFRAG + I4_VIN;
-constexpr int I4_SMEM = I4_BAR_OFF + 2 * I4_NW * I4_D * 8;
+constexpr int I4_STAGE = I4_KS * I4_PAIR_BLOCK;          // 4224 B
+constexpr int I4_SLICE_KSTEPS = I4_KS * I4_GROUP / 16;   // 16 mma k-steps per slice
+constexpr int I4_MAX_RECS = 512;                         // passes one block may touch
+constexpr int I4_STATIC_SMEM = I4_MAX_RECS * 8 + 128;
+
+// nb = mma columns that carry data (2 per token of the widest pass).
+template <int NW, int D>
+struct I4Smem {
+  static constexpr int ring = NW * D * I4_STAGE;
+  static constexpr int bars = NW * D * 8;
+  static constexpr int gateup(int H, int nb) { return ring + bars + (H / 16) * nb * 4 * 8; }
+  // down keeps B fragments for all 8 columns (one slice is small) and the slice inputs
+  static constexpr int down() {
+    return ring + bars + I4_SLICE_KSTEPS * 8 * 4 * 8 + I4_PMAX * I4_KS * I4_GROUP * 4;
+  }
+};
 
 __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;  // (a & b) ^ c
@@ -36,17 +56,18 @@ __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_
   return r;
 }
 
-// 8 nibbles -> the four half2 registers of an m16n8k16 A fragment (exact integers q).
-__device__ __forceinline__ void dequant8(uint32_t w, uint32_t& a0, uint32_t& a1, uint32_t& a2,
-                                         uint32_t& a3) {
+// 8 nibbles -> the four half2 registers of an m16n8k16 A fragment (exact integers q):
+// (u & 0xF) ^ 8 = q + 8 under the fp16 exponent of 1024 gives 1032 + q; the high nibble
+// of a byte gives 1152 + 16 q, rescaled by 1/16.
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
   const uint32_t LO = 0x000F000Fu, HI = 0x00F000F0u;
-  const uint32_t XLO = 0x64086408u, XHI = 0x64806480u;  // fp16 1024 exponent, nibble ^ 8
-  const __half2 off_lo = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const uint32_t XLO = 0x64086408u, XHI = 0x64806480u;
+  const __half2 off_lo = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
   const __half2 sixteenth = __halves2half2(__float2half_rn(0.0625f), __float2half_rn(0.0625f));
   const __half2 off_hi = __halves2half2(__float2half_rn(-72.f), __float2half_rn(-72.f));
   const uint32_t w2 = w >> 8;
-  uint32_t t0 = lop3_and_xor(w, LO, XLO);    // 1032 + q  (rows g,   k 2p / 2p+1)
-  uint32_t t1 = lop3_and_xor(w, HI, XHI);    // 1152 + 16 q (rows g+8)
+  uint32_t t0 = lop3_and_xor(w, LO, XLO);    // rows g,   k 2p / 2p+1
+  uint32_t t1 = lop3_and_xor(w, HI, XHI);    // rows g+8, k 2p / 2p+1
   uint32_t t2 = lop3_and_xor(w2, LO, XLO);   // rows g,   k 2p+8 / 2p+9
   uint32_t t3 = lop3_and_xor(w2, HI, XHI);   // rows g+8, k 2p+8 / 2p+9
   __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&t0), off_lo);
@@ -63,249 +84,417 @@ __device__ __forceinline__ uint32_t pick4(const uint4& v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
-struct I4Unit {
-  int pass, m, ks, ntok, ng;
-  const uint8_t* base;  // first byte of the unit's matrix
-};
-
-template <bool DOWN>
-__device__ __forceinline__ I4Unit i4_unit(const ExpertArgs& a, long long u, int nks, int p_begin,
-                                          const RecGeom& rg, const MatGeom& g) {
-  constexpr int mats = DOWN ? 1 : 2;
-  I4Unit U;
-  U.ks = (int)(u % nks);
-  const long long pm = u / nks;
-  U.m = (int)(pm % mats);
-  const int pi = (int)(pm / mats);
-  U.pass = a.range.order ? a.range.order[p_begin + pi] : p_begin + pi;
-  const int e = a.plan.pass_expert[U.pass];
-  U.ntok = a.plan.pass_ntok[U.pass];
-  U.ng = min(I4_KS, g.ngroup - U.ks * I4_KS);
-  U.base = a.rec_table[e] + (DOWN ? rg.off[2] : (U.m == 0 ? rg.off[0] : rg.off[1]));
-  return U;
+// One task: 32 rows x ng (<= 2) groups from a stage; adds W . x into acc[tile][4].
+// xf: B fragments of the task's first k-step, [k-step][g < nb][p] uint2 (lanes with
+// g >= nb hold zero columns and load nothing).
+__device__ __forceinline__ void i4_task(const uint8_t* st, int ng, const uint2* xf, int lane, int nb,
+                                        float (&acc)[2][4]) {
+  const int gq = lane >> 2;
+  for (int gi = 0; gi < ng; ++gi) {
+    const uint8_t* blk = st + gi * I4_PAIR_BLOCK;
+    const uint4 wa0 = *reinterpret_cast<const uint4*>(blk + lane * 16);
+    const uint4 wb0 = *reinterpret_cast<const uint4*>(blk + 512 + lane * 16);
+    const uint4 wa1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK + lane * 16);
+    const uint4 wb1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK + 512 + lane * 16);
+    const uint32_t sc0 = *reinterpret_cast<const uint32_t*>(blk + 1024 + gq * 4);
+    const uint32_t sc1 = *reinterpret_cast<const uint32_t*>(blk + I4_BLOCK + 1024 + gq * 4);
+    // two independent accumulation chains per tile (even / odd k-steps)
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint2 b = make_uint2(0u, 0u);
+      if (gq < nb) b = xf[(gi * 8 + j) * nb * 4 + lane];
+      uint32_t x0, x1, x2, x3;
+      dequant8(pick4(j < 4 ? wa0 : wb0, j & 3), x0, x1, x2, x3);
+      if (j & 1) mma_16816(d0, x0, x1, x2, x3, b.x, b.y);
+      else mma_16816(c0, x0, x1, x2, x3, b.x, b.y);
+      dequant8(pick4(j < 4 ? wa1 : wb1, j & 3), x0, x1, x2, x3);
+      if (j & 1) mma_16816(d1, x0, x1, x2, x3, b.x, b.y);
+      else mma_16816(c1, x0, x1, x2, x3, b.x, b.y);
+    }
+    const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&sc0));
+    const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&sc1));
+    acc[0][0] = fmaf(s0.x, c0[0] + d0[0], acc[0][0]);
+    acc[0][1] = fmaf(s0.x, c0[1] + d0[1], acc[0][1]);
+    acc[0][2] = fmaf(s0.y, c0[2] + d0[2], acc[0][2]);
+    acc[0][3] = fmaf(s0.y, c0[3] + d0[3], acc[0][3]);
+    acc[1][0] = fmaf(s1.x, c1[0] + d1[0], acc[1][0]);
+    acc[1][1] = fmaf(s1.x, c1[1] + d1[1], acc[1][1]);
+    acc[1][2] = fmaf(s1.y, c1[2] + d1[2], acc[1][2]);
+    acc[1][3] = fmaf(s1.y, c1[3] + d1[3], acc[1][3]);
+  }
 }
 
-template <bool DOWN>
-__global__ void __launch_bounds__((I4_NW + 1) * 32, 1) int4_kernel(ExpertArgs a) {
+// B fragment of mma column n = g (token slot n/2, part n%2) for one k-step: elements
+// v[0], v[1], v[8], v[9] (inputs k0 + 2p, +1, +8, +9), fp16 hi or lo part.
+__device__ __forceinline__ uint2 bfrag(const float* v, int part) {
+  __half hi[4], lo[4];
+  split_half(v[0], hi[0], lo[0]);
+  split_half(v[1], hi[1], lo[1]);
+  split_half(v[8], hi[2], lo[2]);
+  split_half(v[9], hi[3], lo[3]);
+  uint2 r;
+  r.x = part ? pack_half2(lo[0], lo[1]) : pack_half2(hi[0], hi[1]);
+  r.y = part ? pack_half2(lo[2], lo[3]) : pack_half2(hi[2], hi[3]);
+  return r;
+}
+
+// B fragments of one pass's tokens for nks16 k-steps from fp32 values val(ts, k)
+// (k relative to the first k-step), into xf[k-step][g < nb][p].
+template <class Val>
+__device__ __forceinline__ void build_bfrags(uint2* xf, int nks16, int nb, int tid, int nthr, Val val) {
+  const int per = nb * 4;
+  for (int e = tid; e < nks16 * per; e += nthr) {
+    const int kk = e / per, r = e - kk * per, n = r >> 2, pp = r & 3;
+    float f[10];
+    const int kb = kk * 16 + 2 * pp;
+    f[0] = val(n >> 1, kb);
+    f[1] = val(n >> 1, kb + 1);
+    f[8] = val(n >> 1, kb + 8);
+    f[9] = val(n >> 1, kb + 9);
+    xf[e] = bfrag(f, n & 1);
+  }
+}
+
+// ------------------------------------------------------------------ warp-local staging
+// Every warp streams its own tasks: lane 0 starts the bulk copy of task j + D into the
+// ring slot task j has just released, so the block's warps issue copies in parallel and
+// each keeps D tasks in flight.  full[w][d] completes when slot d of warp w has landed.
+__device__ __forceinline__ void stage_issue(int lane, uint32_t full, uint32_t dst, const void* src, uint32_t bytes) {
+  if (lane == 0) {
+    // the slot's previous contents were read through the generic proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(full, bytes);
+    bulk_g2s(dst, src, bytes, full);
+  }
+}
+
+__device__ __forceinline__ int pass_of(const ExpertArgs& a, int p_begin, int pi) {
+  return a.range.order ? __ldcg(a.range.order + p_begin + pi) : p_begin + pi;
+}
+
+// Wait for a full slot (all lanes agree); on a time-out the block is marked aborted.
+template <int D>
+__device__ __forceinline__ bool stage_wait(uint32_t bar, int j, volatile int* abort, const ExpertArgs& a, int lane) {
+  bool ok = !*abort && mbar_wait_bounded(bar, (j / D) & 1, a.budget);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && !*abort && lane == 0) {
+    *abort = 1;
+    atomicOr(a.status, ST_TIMEOUT);
+  }
+  return ok;
+}
+
+// After a time-out: let every copy this warp started land before the block exits.
+template <int D>
+__device__ __forceinline__ void stage_drain(uint32_t full0, int issued, int consumed, const ExpertArgs& a) {
+  for (int j = consumed; j < issued; ++j)
+    if (!mbar_wait_bounded(full0 + 8 * (j % D), (j / D) & 1, a.budget)) atomicOr(a.status, ST_TIMEOUT);
+}
+
+// Record pointers of the passes [pi0, pi1) of this block's range -> smem.
+__device__ __forceinline__ void load_recs(const uint8_t** recs, const ExpertArgs& a, int p_begin, int pi0, int pi1,
+                                          int tid, int nthr) {
+  for (int q = tid; q < pi1 - pi0; q += nthr)
+    recs[q] = a.rec_table[__ldcg(a.plan.pass_expert + pass_of(a, p_begin, pi0 + q))];
+}
+
+// ------------------------------------------------------------------ gate/up
+template <int NW, int D>
+__global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ volatile int s_abort;
-  uint2* xfrag = reinterpret_cast<uint2*>(smem + I4_NW * I4_D * I4_STAGE);
-  float* vin = reinterpret_cast<float*>(smem + I4_NW * I4_D * I4_STAGE + I4_XFRAG);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + I4_BAR_OFF);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + I4_NW * I4_D);
-  const uint32_t stage0 = smem_u32(smem);
-
+  __shared__ const uint8_t* s_rec[I4_MAX_RECS];
+  using SM = I4Smem<NW, D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int mats = DOWN ? 1 : 2;
+  constexpr int nthr = NW * 32;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::ring);
+  uint2* xfrag = reinterpret_cast<uint2*>(smem + SM::ring + SM::bars);
+  const uint32_t full0 = smem_u32(bars + warp * D);
+  const uint32_t ring0 = smem_u32(smem + warp * D * I4_STAGE);
+
   const RecGeom rg = rec_geom(WFMT_INT4, a.H, a.F);
-  const MatGeom g = rg.m[DOWN ? 2 : 0];
-  const int nks = g.nks, ntask = g.ntask;
+  const MatGeom g = rg.m[0];                       // gate and up share the geometry
+  const int NG = g.ngroup, nks = cdiv(NG, I4_KS), ntask = g.ntask;
+  const int per_rb = 2 * nks;                      // tasks of one (pass, row block)
+  const int per_pass = per_rb * ntask;
+  const int rows32 = ntask * 32;
+
+  pdl_wait();  // the plan and x come from the kernels before
   const int p_begin = a.range.p_begin;
-  const int p_end = a.range.p_end < 0 ? a.plan.hdr->n_pass : a.range.p_end;
-  const long long total = (long long)max(0, p_end - p_begin) * mats * nks * ntask;
-  const long long t0 = total * blockIdx.x / gridDim.x;
-  const long long t1 = total * (blockIdx.x + 1) / gridDim.x;
+  const int p_end = a.range.p_end < 0 ? __ldcg(&a.plan.hdr->n_pass) : a.range.p_end;
+  const int total = max(0, p_end - p_begin) * per_pass;
+  const int t0 = (int)((long long)total * blockIdx.x / gridDim.x);
+  const int t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+  const int pi0 = t0 / per_pass, pi1 = t1 > t0 ? (t1 - 1) / per_pass + 1 : pi0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * I4_NW * I4_D; ++i) mbar_init(full0 + 8 * i, 1);
+    for (int i = 0; i < NW * D; ++i) mbar_init(smem_u32(bars + i), 1);
     s_abort = 0;
     mbar_fence_init();
   }
+  load_recs(s_rec, a, p_begin, pi0, pi1, threadIdx.x, nthr);
   __syncthreads();
+  pdl_launch_dependents();
   if (t0 >= t1) return;
 
-  if (warp == I4_NW) {
-    // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    int seq[I4_NW], iss[I4_NW];
-#pragma unroll
-    for (int w = 0; w < I4_NW; ++w) seq[w] = iss[w] = 0;
-    for (long long i = t0; i < t1;) {
-      const long long u = i / ntask;
-      const long long seg_end = min(t1, (u + 1) * ntask);
-      const I4Unit U = i4_unit<DOWN>(a, u, nks, p_begin, rg, g);
-      const uint32_t bytes = (uint32_t)U.ng * I4_PAIR_BLOCK;
-      for (long long r = i; r < seg_end; r += I4_NW) {
-#pragma unroll
-        for (int w = 0; w < I4_NW; ++w) {
-          const long long ti = r + w;
-          if (ti < seg_end) {
-            const int s = seq[w];
-            const int slot = w * I4_D + s % I4_D;
-            if (!s_abort) {
-              bool ok = true;
-              if (s >= I4_D) ok = mbar_wait_bounded(empty0 + 8 * slot, ((s / I4_D) - 1) & 1, a.budget);
-              if (!ok) {
-                s_abort = 1;
-                atomicOr(a.status, ST_TIMEOUT);
-              } else {
-                const int row_task = (int)(ti % ntask);
-                const uint8_t* src =
-                    U.base + ((size_t)row_task * g.ngroup + (size_t)U.ks * I4_KS) * I4_PAIR_BLOCK;
-                mbar_arrive_expect_tx(full0 + 8 * slot, bytes);
-                bulk_g2s(stage0 + slot * I4_STAGE, src, bytes, full0 + 8 * slot);
-                iss[w] = s + 1;
-              }
-            }
-            seq[w] = s + 1;
-          }
-        }
-      }
-      i = seg_end;
+  // this warp's tasks: t0 + warp + NW j, j < nw
+  const int first = t0 + warp;
+  const int nw = first < t1 ? (t1 - first + NW - 1) / NW : 0;
+  int ipi = first / per_pass, irb = (first - ipi * per_pass) / per_rb;   // issue cursor
+  int it = first - ipi * per_pass - irb * per_rb;
+  int j_issue = 0;
+  auto issue_next = [&]() {
+    const int m = it >= nks ? 1 : 0, ks = it - m * nks;
+    const int ng = min(I4_KS, NG - ks * I4_KS);
+    const uint8_t* src = s_rec[ipi - pi0] + (m ? rg.off[1] : rg.off[0]) +
+                         ((size_t)irb * NG + (size_t)ks * I4_KS) * I4_PAIR_BLOCK;
+    const int slot = j_issue % D;
+    stage_issue(lane, full0 + 8 * slot, ring0 + slot * I4_STAGE, src, (uint32_t)ng * I4_PAIR_BLOCK);
+    ++j_issue;
+    it += NW;
+    while (it >= per_rb) {
+      it -= per_rb;
+      if (++irb == ntask) { irb = 0; ++ipi; }
     }
-    // drain: every issued copy has landed before the block may exit
+  };
+  while (j_issue < min(D, nw)) issue_next();
+
+  const int gq = lane >> 2, p = lane & 3;
+  const uint8_t* myring = smem + warp * D * I4_STAGE;
+  int j = 0;                                 // tasks consumed by this warp
+  int ti = first;
+  for (int seg = t0; seg < t1;) {            // segments = one pass each
+    const int pi = seg / per_pass;
+    const int seg_end = min(t1, (pi + 1) * per_pass);
+    const int pass = pass_of(a, p_begin, pi);
+    const int ntok = __ldcg(a.plan.pass_ntok + pass);
+    const int nb = 2 * ntok;
+    int tok[I4_PMAX];
 #pragma unroll
-    for (int w = 0; w < I4_NW; ++w) {
-      for (int d = 0; d < I4_D; ++d) {
-        if (iss[w] > d) {
-          const int last = ((iss[w] - 1 - d) / I4_D) * I4_D + d;  // last fill of this slot
-          if (!mbar_wait_bounded(full0 + 8 * (w * I4_D + d), (last / I4_D) & 1, a.budget))
-            atomicOr(a.status, ST_TIMEOUT);
-        }
+    for (int q = 0; q < I4_PMAX; ++q) tok[q] = q < ntok ? __ldcg(a.plan.pass_tok + pass * I4_PMAX + q) : 0;
+    named_sync(1, nthr);
+    build_bfrags(xfrag, a.H / 16, nb, threadIdx.x, nthr, [&](int ts, int k) {
+      int t = tok[0];
+#pragma unroll
+      for (int q = 1; q < I4_PMAX; ++q)
+        if (ts == q) t = tok[q];
+      return bf16_bits_to_float(a.x[(size_t)t * a.H + k]);
+    });
+    named_sync(1, nthr);
+    float* part = a.part_gu + (size_t)pass * 2 * nks * I4_PMAX * rows32;
+    int local = ti - pi * per_pass;          // compute cursor within the pass
+    int rb = local / per_rb, t = local - rb * per_rb;
+    for (; ti < seg_end; ti += NW) {
+      const int m = t >= nks ? 1 : 0, ks = t - m * nks;
+      const int slot = j % D;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const bool ok = stage_wait<D>(full0 + 8 * slot, j, &s_abort, a, lane);
+      if (ok) {
+        const int ng = min(I4_KS, NG - ks * I4_KS);
+        i4_task(myring + slot * I4_STAGE, ng, xfrag + (size_t)ks * I4_SLICE_KSTEPS * nb * 4, lane, nb, acc);
+      }
+      __syncwarp();
+      ++j;
+      if (ok && j_issue < nw) issue_next();   // refill the slot just read
+      if (ok && p < ntok) {
+        float* dst = part + ((size_t)(m * nks + ks) * I4_PMAX + p) * rows32 + rb * 32;
+        dst[gq] = acc[0][0] + acc[0][1];
+        dst[gq + 8] = acc[0][2] + acc[0][3];
+        dst[gq + 16] = acc[1][0] + acc[1][1];
+        dst[gq + 24] = acc[1][2] + acc[1][3];
+      }
+      t += NW;                               // advance the compute cursor by NW tasks
+      while (t >= per_rb) {
+        t -= per_rb;
+        ++rb;
       }
     }
+    seg = seg_end;
+  }
+  if (s_abort && lane == 0) stage_drain<D>(full0, j_issue, j, a);
+}
+
+// ------------------------------------------------------------------ down
+template <int NW, int D>
+__global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ volatile int s_abort;
+  __shared__ const uint8_t* s_rec[I4_MAX_RECS];
+  using SM = I4Smem<NW, D>;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::ring);
+  uint2* xfrag = reinterpret_cast<uint2*>(smem + SM::ring + SM::bars);
+  float* vin = reinterpret_cast<float*>(smem + SM::ring + SM::bars + I4_SLICE_KSTEPS * 8 * 4 * 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars + warp * D);
+  const uint32_t ring0 = smem_u32(smem + warp * D * I4_STAGE);
+  constexpr int nthr = NW * 32;
+
+  const RecGeom rg = rec_geom(WFMT_INT4, a.H, a.F);
+  const MatGeom g = rg.m[2];
+  const int NG = g.ngroup, nks = cdiv(NG, I4_KS), ntask = g.ntask;
+  const int rows32 = ntask * 32;
+  const int nks_gu = cdiv(rg.m[0].ngroup, I4_KS), rows32_f = rg.m[0].ntask * 32;
+  const int per_pass = nks * ntask;
+
+  // The plan is older than the gate/up kernel, which waited for it before it let this
+  // kernel start, so the weights stream before the gate/up partials are ready.
+  const int p_begin = a.range.p_begin;
+  const int p_end = a.range.p_end < 0 ? __ldcg(&a.plan.hdr->n_pass) : a.range.p_end;
+  const int total = max(0, p_end - p_begin) * per_pass;
+  const int t0 = (int)((long long)total * blockIdx.x / gridDim.x);
+  const int t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+  const int pi0 = t0 / per_pass, pi1 = t1 > t0 ? (t1 - 1) / per_pass + 1 : pi0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW * D; ++i) mbar_init(smem_u32(bars + i), 1);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  load_recs(s_rec, a, p_begin, pi0, pi1, threadIdx.x, nthr);
+  __syncthreads();
+  if (t0 >= t1) {
+    pdl_wait();
+    pdl_launch_dependents();
     return;
   }
 
-  // -------------------------------------------------------------- consumers
-  const int gq = lane >> 2, p = lane & 3;
-  int seq = 0;
-  // gate/up partial geometry (down reads it)
-  const MatGeom gg = rg.m[0];
-  const int rows32_gu = gg.ntask * 32;
-  for (long long i = t0; i < t1;) {
-    const long long u = i / ntask;
-    const long long seg_end = min(t1, (u + 1) * ntask);
-    const I4Unit U = i4_unit<DOWN>(a, u, nks, p_begin, rg, g);
-    const int* toks = a.plan.pass_tok + U.pass * I4_PMAX;
+  const int first = t0 + warp;
+  const int nw = first < t1 ? (t1 - first + NW - 1) / NW : 0;
+  int iu = first / ntask, irb = first - iu * ntask;   // issue cursor: unit (pass, k-slice), row block
+  int j_issue = 0;
+  auto issue_next = [&]() {
+    const int ipi = iu / nks, iks = iu - ipi * nks;
+    const int ng = min(I4_KS, NG - iks * I4_KS);
+    const uint8_t* src = s_rec[ipi - pi0] + rg.off[2] + ((size_t)irb * NG + (size_t)iks * I4_KS) * I4_PAIR_BLOCK;
+    const int slot = j_issue % D;
+    stage_issue(lane, full0 + 8 * slot, ring0 + slot * I4_STAGE, src, (uint32_t)ng * I4_PAIR_BLOCK);
+    ++j_issue;
+    irb += NW;
+    while (irb >= ntask) {
+      irb -= ntask;
+      ++iu;
+    }
+  };
+  while (j_issue < min(D, nw)) issue_next();
 
-    named_sync(1, I4_NW * 32);
-    // slice input, fp32 [slot][512]: x (gate/up) or h = silu(g) * u (down)
-    const int kbase = U.ks * (I4_KS * I4_GROUP);
-    const int kvalid = U.ng * I4_GROUP;
-    for (int e = threadIdx.x; e < U.ntok * I4_KS * I4_GROUP; e += I4_NW * 32) {
-      const int ts = e / (I4_KS * I4_GROUP), kk = e % (I4_KS * I4_GROUP);
+  pdl_wait();  // the gate/up partials come from the kernel before
+  pdl_launch_dependents();
+  const int gq = lane >> 2, p = lane & 3;
+  const uint8_t* myring = smem + warp * D * I4_STAGE;
+  int j = 0;
+  int ti = first;
+  for (int seg = t0; seg < t1;) {  // segments = one unit (pass, k-slice) each
+    const int u = seg / ntask;
+    const int seg_end = min(t1, (u + 1) * ntask);
+    const int pi = u / nks, ks = u - pi * nks;
+    const int pass = pass_of(a, p_begin, pi);
+    const int ntok = __ldcg(a.plan.pass_ntok + pass);
+    const int nb = 2 * ntok;
+    const int ng = min(I4_KS, NG - ks * I4_KS);
+    const int kbase = ks * I4_KS * I4_GROUP, kvalid = ng * I4_GROUP;
+    named_sync(1, nthr);
+    // h of this slice: silu(g) * u, the gate / up partials added in k-slice order
+    for (int e = threadIdx.x; e < ntok * I4_KS * I4_GROUP; e += nthr) {
+      const int ts = e / (I4_KS * I4_GROUP), kk = e - ts * (I4_KS * I4_GROUP);
       float v = 0.f;
       if (kk < kvalid) {
-        const int k = kbase + kk;
-        if (!DOWN) {
-          v = bf16_bits_to_float(a.x[(size_t)toks[ts] * a.H + k]);
-        } else {
-          const float* pg = a.part_gu + (((size_t)(U.pass * 2 + 0) * gg.nks) * rows32_gu + k) * I4_PMAX + ts;
-          const float* pu = a.part_gu + (((size_t)(U.pass * 2 + 1) * gg.nks) * rows32_gu + k) * I4_PMAX + ts;
-          const size_t stride = (size_t)rows32_gu * I4_PMAX;
-          float gs = 0.f, us = 0.f;
-#pragma unroll 4
-          for (int s2 = 0; s2 < gg.nks; ++s2) {
-            gs += __ldcg(pg + s2 * stride);
-            us += __ldcg(pu + s2 * stride);
+        const size_t stride = (size_t)I4_PMAX * rows32_f;
+        const float* pg = a.part_gu + ((size_t)pass * 2 * nks_gu * I4_PMAX + ts) * rows32_f + kbase + kk;
+        const float* pu = pg + (size_t)nks_gu * stride;
+        float gs = 0.f, us = 0.f;
+        for (int s0 = 0; s0 < nks_gu; s0 += 8) {
+          float gv[8], uv[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const bool in = s0 + q < nks_gu;
+            gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * stride) : 0.f;
+            uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * stride) : 0.f;
           }
-          v = gs / (1.f + expf(-gs)) * us;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            gs += gv[q];
+            us += uv[q];
+          }
         }
+        v = gs / (1.f + expf(-gs)) * us;
       }
       vin[e] = v;
     }
-    named_sync(1, I4_NW * 32);
-    for (int e = threadIdx.x; e < I4_KSTEPS * 32; e += I4_NW * 32) {
-      const int kk = e >> 5, ln = e & 31;
-      const int n = ln >> 2, pp = ln & 3;
-      const int ts = n >> 1, part = n & 1;
-      uint2 v = make_uint2(0u, 0u);
-      if (ts < U.ntok) {
-        const float* src = vin + ts * (I4_KS * I4_GROUP) + kk * 16 + 2 * pp;
-        __half hi[4], lo[4];
-        split_half(src[0], hi[0], lo[0]);
-        split_half(src[1], hi[1], lo[1]);
-        split_half(src[8], hi[2], lo[2]);
-        split_half(src[9], hi[3], lo[3]);
-        v.x = part ? pack_half2(lo[0], lo[1]) : pack_half2(hi[0], hi[1]);
-        v.y = part ? pack_half2(lo[2], lo[3]) : pack_half2(hi[2], hi[3]);
-      }
-      xfrag[e] = v;
-    }
-    named_sync(1, I4_NW * 32);
-
-    const int nb = 2 * U.ntok;  // mma columns that carry data
-    for (long long ti = i + warp; ti < seg_end; ti += I4_NW) {
-      const int slot = warp * I4_D + seq % I4_D;
-      bool ok = !s_abort && mbar_wait_bounded(full0 + 8 * slot, (seq / I4_D) & 1, a.budget);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
-        const uint8_t* st = smem + slot * I4_STAGE;
-        float acc[2][4];
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[t][c] = 0.f;
-        for (int gi = 0; gi < U.ng; ++gi) {
-          const uint8_t* blk = st + gi * I4_PAIR_BLOCK;
-          const uint4 wa0 = *reinterpret_cast<const uint4*>(blk + lane * 16);
-          const uint4 wb0 = *reinterpret_cast<const uint4*>(blk + 512 + lane * 16);
-          const uint4 wa1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK + lane * 16);
-          const uint4 wb1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK + 512 + lane * 16);
-          const uint32_t sc0 = *reinterpret_cast<const uint32_t*>(blk + 1024 + gq * 4);
-          const uint32_t sc1 = *reinterpret_cast<const uint32_t*>(blk + I4_BLOCK + 1024 + gq * 4);
-          float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint2 b = make_uint2(0u, 0u);
-            if (gq < nb) b = xfrag[(gi * 8 + j) * 32 + lane];
-            uint32_t x0, x1, x2, x3;
-            dequant8(pick4(j < 4 ? wa0 : wb0, j & 3), x0, x1, x2, x3);
-            mma_16816(c0, x0, x1, x2, x3, b.x, b.y);
-            dequant8(pick4(j < 4 ? wa1 : wb1, j & 3), x0, x1, x2, x3);
-            mma_16816(c1, x0, x1, x2, x3, b.x, b.y);
-          }
-          const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&sc0));
-          const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&sc1));
-          acc[0][0] = fmaf(s0.x, c0[0], acc[0][0]);
-          acc[0][1] = fmaf(s0.x, c0[1], acc[0][1]);
-          acc[0][2] = fmaf(s0.y, c0[2], acc[0][2]);
-          acc[0][3] = fmaf(s0.y, c0[3], acc[0][3]);
-          acc[1][0] = fmaf(s1.x, c1[0], acc[1][0]);
-          acc[1][1] = fmaf(s1.x, c1[1], acc[1][1]);
-          acc[1][2] = fmaf(s1.y, c1[2], acc[1][2]);
-          acc[1][3] = fmaf(s1.y, c1[3], acc[1][3]);
-        }
-        if (p < U.ntok) {
-          const int row_task = (int)(ti % ntask);
-          const int rows32 = ntask * 32;
-          float* dst;
-          if (!DOWN)
-            dst = a.part_gu + ((size_t)(U.pass * 2 + U.m) * nks + U.ks) * rows32 * I4_PMAX;
-          else
-            dst = a.part_d + ((size_t)U.pass * nks + U.ks) * rows32 * I4_PMAX;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int r = row_task * 32 + t * 16 + gq;
-            dst[(size_t)r * I4_PMAX + p] = acc[t][0] + acc[t][1];
-            dst[(size_t)(r + 8) * I4_PMAX + p] = acc[t][2] + acc[t][3];
-          }
-        }
-      } else if (!s_abort) {
-        if (lane == 0) { s_abort = 1; atomicOr(a.status, ST_TIMEOUT); }
-      }
+    named_sync(1, nthr);
+    build_bfrags(xfrag, I4_SLICE_KSTEPS, nb, threadIdx.x, nthr,
+                 [&](int ts, int k) { return vin[ts * (I4_KS * I4_GROUP) + k]; });
+    named_sync(1, nthr);
+    float* dst0 = a.part_d + ((size_t)pass * nks + ks) * I4_PMAX * rows32;
+    for (; ti < seg_end; ti += NW) {
+      const int rb = ti - u * ntask;
+      const int slot = j % D;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const bool ok = stage_wait<D>(full0 + 8 * slot, j, &s_abort, a, lane);
+      if (ok) i4_task(myring + slot * I4_STAGE, ng, xfrag, lane, nb, acc);
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-      ++seq;
+      ++j;
+      if (ok && j_issue < nw) issue_next();
+      if (ok && p < ntok) {
+        float* dst = dst0 + (size_t)p * rows32 + rb * 32;
+        dst[gq] = acc[0][0] + acc[0][1];
+        dst[gq + 8] = acc[0][2] + acc[0][3];
+        dst[gq + 16] = acc[1][0] + acc[1][1];
+        dst[gq + 24] = acc[1][2] + acc[1][3];
+      }
     }
-    i = seg_end;
+    seg = seg_end;
   }
+  if (s_abort && lane == 0) stage_drain<D>(full0, j_issue, j, a);
 }
 
-cudaError_t int4_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(int4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, I4_SMEM);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(int4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, I4_SMEM);
+// ------------------------------------------------------------------ launch configuration
+// 16 warps; ring depth 3 when the B fragments of the widest pass (nb columns, all of K)
+// leave room for it, else 2; wide inputs with 4-token passes drop to 8 warps.
+struct I4Launch {
+  int nw, d;
+  size_t smem_gu, smem_down;
+};
+
+static I4Launch i4_config(int H, int max_tokens) {
+  const int nb = 2 * std::min(max_tokens, I4_PMAX);
+  const size_t cap = 227 * 1024 - I4_STATIC_SMEM;
+  if ((size_t)I4Smem<16, 3>::gateup(H, nb) <= cap)
+    return {16, 3, (size_t)I4Smem<16, 3>::gateup(H, nb), (size_t)I4Smem<16, 3>::down()};
+  if ((size_t)I4Smem<16, 2>::gateup(H, nb) <= cap)
+    return {16, 2, (size_t)I4Smem<16, 2>::gateup(H, nb), (size_t)I4Smem<16, 2>::down()};
+  return {8, 2, (size_t)I4Smem<8, 2>::gateup(H, nb), (size_t)I4Smem<8, 2>::down()};
+}
+
+template <int NW, int D>
+static cudaError_t i4_attrs(const I4Launch& c) {
+  cudaError_t e = cudaFuncSetAttribute(int4_gateup_kernel<NW, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)c.smem_gu);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(int4_down_kernel<NW, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem_down);
+  return e;
+}
+
+cudaError_t int4_set_attributes(int H, int max_tokens) {
+  const I4Launch c = i4_config(H, max_tokens);
+  if (c.nw == 16 && c.d == 3) return i4_attrs<16, 3>(c);
+  if (c.nw == 16) return i4_attrs<16, 2>(c);
+  return i4_attrs<8, 2>(c);
 }
 
 cudaError_t launch_int4_gateup(const ExpertArgs& a, int grid, cudaStream_t s) {
-  int4_kernel<false><<<grid, (I4_NW + 1) * 32, I4_SMEM, s>>>(a);
-  return cudaGetLastError();
+  const I4Launch c = i4_config(a.H, a.max_tokens);
+  if (c.nw == 16 && c.d == 3) return launch_pdl(int4_gateup_kernel<16, 3>, grid, 16 * 32, c.smem_gu, s, a);
+  if (c.nw == 16) return launch_pdl(int4_gateup_kernel<16, 2>, grid, 16 * 32, c.smem_gu, s, a);
+  return launch_pdl(int4_gateup_kernel<8, 2>, grid, 8 * 32, c.smem_gu, s, a);
 }
+
 cudaError_t launch_int4_down(const ExpertArgs& a, int grid, cudaStream_t s) {
-  int4_kernel<true><<<grid, (I4_NW + 1) * 32, I4_SMEM, s>>>(a);
-  return cudaGetLastError();
+  const I4Launch c = i4_config(a.H, a.max_tokens);
+  if (c.nw == 16 && c.d == 3) return launch_pdl(int4_down_kernel<16, 3>, grid, 16 * 32, c.smem_down, s, a);
+  if (c.nw == 16) return launch_pdl(int4_down_kernel<16, 2>, grid, 16 * 32, c.smem_down, s, a);
+  return launch_pdl(int4_down_kernel<8, 2>, grid, 8 * 32, c.smem_down, s, a);
 }
 
 }  // namespace moe

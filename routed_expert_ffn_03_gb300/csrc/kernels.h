@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <utility>
 #include <cstdint>
 
 #include "layout.h"
@@ -18,8 +19,15 @@ struct DevCounters {           // updated on the device by the router's last blo
   unsigned long long forwards, tokens, lookups, bytes_touched, bytes_router;
 };
 
+constexpr int ROUTER_FUSED_MAXT = 256;
+
 struct RouterArgs {
-  const uint16_t* x;     // bf16 [T][H]
+  const uint16_t* x;     // bf16 [T][H] router input (when xres is null)
+  const float* xres;     // fused stack step: fp32 residual [T][H] (null: not fused)
+  const float* yprev;    //   previous layer's output [T][H] or null
+  float* xres_out;       //   x + yprev written here by the last block
+  uint16_t* xn_out;      //   bf16(rmsnorm(x + yprev)) written here by the last block
+  float eps;
   const float* W;        // [E][H]
   int T, H, E, k, kind, pmax, has_shared;
   float* partial;        // [E][nch][T]
@@ -44,14 +52,17 @@ struct PassRange {
 struct ExpertArgs {
   const uint8_t* const* rec_table;  // [E + 1] record pointers (E = shared expert)
   PlanPtrs plan;
-  int H, F, E, T;
+  int H, F, E, T, max_tokens;
   const uint16_t* x;                // bf16 [T][H] (gate/up input)
-  float* part_gu;                   // [max_pass][2][nks_gu][rows32(F)][pmax]
-  float* part_d;                    // [max_pass][nks_d][rows32(H)][pmax]
+  float* part_gu;                   // [max_pass][2][nks_gu][pmax][rows32(F)] gate/up partials
+  float* h;                         // int4: [max_pass][pmax][rows32(F)] SwiGLU outputs
+  float* part_d;                    // [max_pass][nks_d][pmax][rows32(H)]
   PassRange range;
   uint32_t* status;
   unsigned long long budget;
 };
+cudaError_t int4_set_attributes(int H, int max_tokens);
+cudaError_t rvq_set_attributes();
 cudaError_t launch_int4_gateup(const ExpertArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_int4_down(const ExpertArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_rvq_gateup(const ExpertArgs& a, int grid, cudaStream_t s);
@@ -71,5 +82,23 @@ cudaError_t launch_wait_timeout(uint32_t* status, unsigned long long budget, cud
 
 cudaError_t launch_repack(int wfmt, const uint8_t* blob, int H, int F, uint8_t* rec,
                           cudaStream_t stream);
+
+// Launch with programmatic stream serialisation (the kernel calls pdl_wait before it reads
+// what the previous kernel wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 }  // namespace moe

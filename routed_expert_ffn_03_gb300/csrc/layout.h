@@ -49,7 +49,7 @@ constexpr int ROWS_PER_TASK = 32;   // both formats: one warp task covers 32 row
 constexpr int I4_GROUP = 128;
 constexpr int I4_BLOCK = 1056;           // one 16-row tile x one group
 constexpr int I4_PAIR_BLOCK = 2 * I4_BLOCK;
-constexpr int I4_KS = 4;                 // groups per k-slice (512 inputs)
+constexpr int I4_KS = 2;                 // groups per k-slice / task (256 inputs)
 constexpr int I4_PMAX = 4;               // tokens per pass (hi/lo fill the 8 mma columns)
 
 // RVQ

@@ -7,9 +7,14 @@
 // divided by their sum.  Both are monotone in the logit, so the top-k is taken on the
 // fp32 logits; equal logits rank the lower expert id first.
 //
+// Optional fused stack step (x, y_prev given): every block computes the token's inverse
+// RMS of x + y_prev with the same fixed-order reduction as the residual_rmsnorm kernel and
+// uses xn = bf16((x + y_prev) * inv) as the router input; the last block, once every block
+// has read x, writes x + y_prev back to x and xn out for the expert kernels.
 // Phase 1 (all blocks): each warp owns (expert e, 512-wide chunk c of H) and writes the
 // partial dot products of all T tokens.  Phase 2 (the block that arrives last, found
-// with an atomic ticket; no block waits on another): sums the partials in chunk order,
+// with an atomic ticket; no block waits on another): sums the partials in chunk order
+// (all (token, expert) pairs in parallel),
 // selects the top-k per token (one warp per token), and buckets the (token, rank) pairs
 // by expert into "passes" of up to pmax tokens: routed experts in ascending id, tokens
 // ascending, then the shared expert.
@@ -29,12 +34,42 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+constexpr int LOGIT_SMEM = 8192;  // floats of logits staged per chunk of tokens
+
 __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
   extern __shared__ int sm[];
+  __shared__ float s_inv[ROUTER_FUSED_MAXT];
+  __shared__ float s_red[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int nch = cdiv(a.H, RCH);
   const int nitems = a.E * nch;
+  const bool fused = a.xres != nullptr;
+
+  pdl_wait();  // x (and the residual) come from the kernels before
+  pdl_launch_dependents();
+  if (fused) {
+    for (int t = 0; t < a.T; ++t) {
+      const float inv = block_inv_rms(a.xres + (size_t)t * a.H, a.yprev ? a.yprev + (size_t)t * a.H : nullptr,
+                                      a.H, a.eps, s_red);
+      if (threadIdx.x == 0) s_inv[t] = inv;
+    }
+    __syncthreads();
+  }
+
+  if (fused) {
+    // xn is not read by this kernel: each block writes a disjoint slice of it
+    const int per = cdiv(a.H, gridDim.x);
+    for (int t = 0; t < a.T; ++t) {
+      const float inv = s_inv[t];
+      for (int h = blockIdx.x * per + threadIdx.x; h < min(a.H, (blockIdx.x + 1) * per); h += blockDim.x) {
+        const size_t o = (size_t)t * a.H + h;
+        float v = __ldcg(a.xres + o);
+        if (a.yprev) v += __ldcg(a.yprev + o);
+        a.xn_out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(v * inv));
+      }
+    }
+  }
 
   // ---------------- phase 1: partial logits
   for (int item = blockIdx.x * nwarps + warp; item < nitems; item += gridDim.x * nwarps) {
@@ -51,11 +86,30 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 #pragma unroll
         for (int tt = 0; tt < 8; ++tt) {
           if (tt < nt) {
-            const uint2 xb = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)(t0 + tt) * a.H + h));
-            acc[tt] = fmaf(wv.x, __uint_as_float(xb.x << 16), acc[tt]);
-            acc[tt] = fmaf(wv.y, __uint_as_float(xb.x & 0xffff0000u), acc[tt]);
-            acc[tt] = fmaf(wv.z, __uint_as_float(xb.y << 16), acc[tt]);
-            acc[tt] = fmaf(wv.w, __uint_as_float(xb.y & 0xffff0000u), acc[tt]);
+            float x0, x1, x2, x3;
+            if (fused) {
+              const size_t o = (size_t)(t0 + tt) * a.H + h;
+              float4 v = __ldcg(reinterpret_cast<const float4*>(a.xres + o));
+              if (a.yprev) {
+                const float4 y = __ldcg(reinterpret_cast<const float4*>(a.yprev + o));
+                v.x += y.x; v.y += y.y; v.z += y.z; v.w += y.w;
+              }
+              const float inv = s_inv[t0 + tt];
+              x0 = __bfloat162float(__float2bfloat16_rn(v.x * inv));
+              x1 = __bfloat162float(__float2bfloat16_rn(v.y * inv));
+              x2 = __bfloat162float(__float2bfloat16_rn(v.z * inv));
+              x3 = __bfloat162float(__float2bfloat16_rn(v.w * inv));
+            } else {
+              const uint2 xb = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)(t0 + tt) * a.H + h));
+              x0 = __uint_as_float(xb.x << 16);
+              x1 = __uint_as_float(xb.x & 0xffff0000u);
+              x2 = __uint_as_float(xb.y << 16);
+              x3 = __uint_as_float(xb.y & 0xffff0000u);
+            }
+            acc[tt] = fmaf(wv.x, x0, acc[tt]);
+            acc[tt] = fmaf(wv.y, x1, acc[tt]);
+            acc[tt] = fmaf(wv.z, x2, acc[tt]);
+            acc[tt] = fmaf(wv.w, x3, acc[tt]);
           }
         }
       }
@@ -80,63 +134,79 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
   __threadfence();
 
   const int E = a.E, T = a.T, k = a.k, pmax = a.pmax;
-  int* s_cnt = sm;            // [E]
-  int* s_off = s_cnt + E;     // [E]
-  int* s_idx = s_off + E;     // [T*k]
-  int* s_pos = s_idx + T * k; // [T*k]
+  float* slog = reinterpret_cast<float*>(sm);   // [tc][E]
+  int* s_cnt = sm + LOGIT_SMEM;                 // [E]
+  int* s_off = s_cnt + E;                       // [E]
+  int* s_idx = s_off + E;                       // [T*k]
+  int* s_pos = s_idx + T * k;                   // [T*k]
 
-  // ---------------- phase 2a: logits, top-k, weights (one warp per token)
-  for (int t = warp; t < T; t += nwarps) {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      float s = -INFINITY;
-      if (e < E) {
-        s = 0.f;
-        for (int c = 0; c < nch; ++c) s += __ldcg(a.partial + ((size_t)e * nch + c) * T + t);
-      }
-      v[i] = s;
+  if (fused && a.yprev) {
+    // every block has read x: now the residual is updated
+    for (int i = threadIdx.x; i < T * a.H; i += blockDim.x) a.xres_out[i] = a.xres[i] + a.yprev[i];
+  }
+
+  // ---------------- phase 2a: logits (all (t, e) in parallel), then top-k per token
+  const int tc = max(1, min(T, LOGIT_SMEM / E));
+  for (int tb = 0; tb < T; tb += tc) {
+    const int nt = min(tc, T - tb);
+    for (int q = threadIdx.x; q < nt * E; q += blockDim.x) {
+      const int tl = q / E, e = q % E;
+      const float* pp = a.partial + (size_t)e * nch * T + tb + tl;
+      float s = 0.f;
+#pragma unroll 8
+      for (int c = 0; c < nch; ++c) s += __ldcg(pp + (size_t)c * T);
+      slog[tl * E + e] = s;
     }
-    int my_e = 0;
-    float my_l = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+    __syncthreads();
+    for (int tl = warp; tl < nt; tl += nwarps) {
+      const int t = tb + tl;
+      float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
+        v[i] = e < E ? slog[tl * E + e] : -INFINITY;
       }
+      int my_e = 0;
+      float my_l = 0.f;
+      for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        for (int i = 0; i < 32; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (lane + 32 * i == be) v[i] = -INFINITY;
+        if (lane == j) { my_e = be; my_l = bv; }
       }
+      // weights over the k selected (rank order = lane order)
+      const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+      float num = 0.f;
+      if (lane < k) {
+        if (a.kind == 0) num = expf(my_l - lmax);
+        else num = 1.f / (1.f + expf(-my_l));
+      }
+      float den = num;
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (lane + 32 * i == be) v[i] = -INFINITY;
-      if (lane == j) { my_e = be; my_l = bv; }
+      for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      if (lane < k) {
+        const float w = num / den;
+        a.plan.idx[t * k + lane] = my_e;
+        a.plan.w[t * k + lane] = w;
+        a.store_idx[t * k + lane] = my_e;
+        a.store_w[t * k + lane] = w;
+        s_idx[t * k + lane] = my_e;
+      }
     }
-    // weights over the k selected (rank order = lane order)
-    const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-    float num = 0.f;
-    if (lane < k) {
-      if (a.kind == 0) num = expf(my_l - lmax);
-      else num = 1.f / (1.f + expf(-my_l));
-    }
-    float den = num;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (lane < k) {
-      const float w = num / den;
-      a.plan.idx[t * k + lane] = my_e;
-      a.plan.w[t * k + lane] = w;
-      a.store_idx[t * k + lane] = my_e;
-      a.store_w[t * k + lane] = w;
-      s_idx[t * k + lane] = my_e;
-    }
+    __syncthreads();
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
@@ -184,11 +254,11 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
       a.plan.hdr->T = T;
       s_routed = tot_p;
       DevCounters* dc = a.counters;
-      dc->forwards += 1;
-      dc->tokens += (unsigned long long)T;
-      dc->lookups += (unsigned long long)tot_u;
-      dc->bytes_touched += (unsigned long long)(tot_u + (a.has_shared ? 1 : 0)) * a.record_bytes;
-      dc->bytes_router += (unsigned long long)E * a.H * 4ull;
+      atomicAdd(&dc->forwards, 1ull);
+      atomicAdd(&dc->tokens, (unsigned long long)T);
+      atomicAdd(&dc->lookups, (unsigned long long)tot_u);
+      atomicAdd(&dc->bytes_touched, (unsigned long long)(tot_u + (a.has_shared ? 1 : 0)) * a.record_bytes);
+      atomicAdd(&dc->bytes_router, (unsigned long long)E * a.H * 4ull);
     }
   }
   __syncthreads();
@@ -234,9 +304,8 @@ cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s) {
   const int nitems = a.E * nch;
   int grid = cdiv(nitems, 8);
   grid = std::max(1, std::min(grid, 4 * num_sms));
-  const size_t smem = (size_t)(2 * a.E + 2 * a.T * a.k) * sizeof(int);
-  router_kernel<<<grid, 256, smem, s>>>(a);
-  return cudaGetLastError();
+  const size_t smem = (size_t)(LOGIT_SMEM + 2 * a.E + 2 * a.T * a.k) * sizeof(int);
+  return launch_pdl(router_kernel, grid, 256, smem, s, a);
 }
 
 }  // namespace moe

@@ -60,17 +60,21 @@ def lib():
     L.moe_expert_blob_bytes.restype = ctypes.c_size_t
     L.moe_forward.argtypes = [vp, i, vp, vp, i, vp]
     L.moe_get_routing.argtypes = [vp, i, vp, vp, ctypes.POINTER(i)]
+    L.moe_forward_residual.argtypes = [vp, i, vp, vp, vp, vp, i, ctypes.c_float, vp]
     L.moe_residual_rmsnorm.argtypes = [vp, vp, vp, vp, i, ctypes.c_float, vp]
     L.moe_stats.argtypes = [vp, ctypes.POINTER(Stats)]
     L.moe_reset_stats.argtypes = [vp]
     L.moe_destroy.argtypes = [vp]
     L.moe_strerror.argtypes = [i]
     L.moe_strerror.restype = ctypes.c_char_p
+    L.moe_profile.argtypes = [vp, i]
+    L.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i)]
     L.moe_debug_fail_copies.argtypes = [vp, i]
     L.moe_debug_wait_timeout.argtypes = [vp, u64, vp, ctypes.POINTER(i)]
     for name in ("moe_create", "moe_register_router", "moe_register_expert", "moe_forward",
                  "moe_get_routing", "moe_residual_rmsnorm", "moe_stats", "moe_reset_stats",
-                 "moe_destroy", "moe_debug_fail_copies", "moe_debug_wait_timeout"):
+                 "moe_destroy", "moe_debug_fail_copies", "moe_debug_wait_timeout",
+                 "moe_profile", "moe_profile_read", "moe_forward_residual"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -160,6 +164,13 @@ class Context:
         self._check(lib().moe_forward(self._h, layer, _ptr(x_bf16), _ptr(out), T, _stream(stream)),
                     "moe_forward")
 
+    def forward_residual(self, layer, x, y_prev, xn, y, T=None, eps=1e-6, stream=None):
+        """Fused stack step: x += y_prev (if given); xn = bf16(rmsnorm(x)); y = layer(xn)."""
+        if T is None:
+            T = x.shape[0]
+        self._check(lib().moe_forward_residual(self._h, layer, _ptr(x), _ptr(y_prev), _ptr(xn), _ptr(y), T,
+                                               float(eps), _stream(stream)), "moe_forward_residual")
+
     def residual_rmsnorm(self, x, y, xn, T=None, eps=1e-6, stream=None):
         if T is None:
             T = x.shape[0]
@@ -190,6 +201,17 @@ class Context:
 
     def reset_stats(self):
         self._check(lib().moe_reset_stats(self._h), "moe_reset_stats")
+
+    # -- measurement
+    def profile(self, enable=True):
+        self._check(lib().moe_profile(self._h, 1 if enable else 0), "moe_profile")
+
+    def profile_read(self):
+        """(ms[router, gateup, down, combine] summed over recorded layers, n_layers)."""
+        ms = (ctypes.c_double * 4)()
+        n = ctypes.c_int(0)
+        self._check(lib().moe_profile_read(self._h, ms, ctypes.byref(n)), "moe_profile_read")
+        return list(ms), n.value
 
     # -- failure injection (host side)
     def debug_fail_copies(self, n):

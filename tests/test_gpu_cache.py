@@ -165,3 +165,26 @@ def test_bounded_device_wait_reports_timeout():
     st, _ = ctx.stats_status()               # the check does not poison the context
     assert st == M.OK
     ctx.close()
+
+
+@pytest.mark.parametrize("spec", [SPEC, SPEC4])
+def test_fused_stack_step_equals_separate_calls(spec):
+    """moe_forward_residual == moe_residual_rmsnorm + moe_forward, bit for bit."""
+    import torch
+    ctx = make_context(spec, 1)
+    seq = _tokens(spec, 5)
+    ref, _ = _stack_run(ctx, spec, seq)
+    outs = []
+    T, H = 1, spec.H
+    x = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    y = torch.zeros_like(x)
+    xn = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    for xb in seq:
+        x.copy_(torch.from_numpy(S.bf16_bits_to_f32(xb)))
+        for l in range(spec.layers):
+            ctx.forward_residual(l, x, None if l == 0 else y, xn, y, T)
+        ctx.residual_rmsnorm(x, y, xn)
+        torch.cuda.synchronize()
+        outs.append(x.cpu().numpy().copy())
+    ctx.close()
+    np.testing.assert_array_equal(np.stack(outs), ref)

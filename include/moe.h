@@ -177,6 +177,25 @@ moe_status moe_destroy(moe_ctx* ctx);
 
 const char* moe_strerror(moe_status s);
 
+/* Routing of T tokens without allocating anything (no counterpart in the pages).
+ * For callers that cannot allocate device memory when they route: code recording a CUDA
+ * graph (cudaMalloc is not allowed during stream capture), an engine whose own memory
+ * pool already holds the free device memory, or a host application whose plugin rules
+ * forbid allocation.  It runs the router of moe_forward (router GEMV, top-k, softmax
+ * renormalised or sigmoid normalised weights) on x bf16 [T,H] with W fp32 [E,H] (device
+ * pointers, no context needed) and writes idx int32 [T,k] and w fp32 [T,k] (device) on
+ * `stream`, the same values moe_forward records for moe_get_routing.
+ * Scratch: one 1 MiB device array per device, held for the life of the process; calls
+ * whose partial logits (E * ceil(H/512) * T floats) and plan do not fit return
+ * MOE_EINVAL.  Limits otherwise as moe_config (T <= 256, E <= 1024, k <= 32, H % 8 == 0).
+ * The first call on a device sets that device up (looks up the array's device address
+ * and the kernel's shared-memory limit); make it before any stream capture.  Every call
+ * shares the array and it keeps the last call's contents (the ticket it needs at zero is
+ * cleared by each call on its stream), so calls that overlap on the GPU (different
+ * streams, or other threads) race: order them.  Uses the current device. */
+moe_status moe_route_noalloc(const uint16_t* x_bf16, const float* W, int T, int H, int E, int k, int router,
+                             int* idx, float* w, void* stream);
+
 /* ---- measurement (no counterpart in the pages) ---- */
 
 /* Per-kernel timing: when enabled, moe_forward records CUDA events (timing enabled) on its

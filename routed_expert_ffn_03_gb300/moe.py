@@ -61,6 +61,7 @@ def lib():
     L.moe_forward.argtypes = [vp, i, vp, vp, i, vp]
     L.moe_get_routing.argtypes = [vp, i, vp, vp, ctypes.POINTER(i)]
     L.moe_forward_residual.argtypes = [vp, i, vp, vp, vp, vp, i, ctypes.c_float, vp]
+    L.moe_route_noalloc.argtypes = [vp, vp, i, i, i, i, i, vp, vp, vp]
     L.moe_residual_rmsnorm.argtypes = [vp, vp, vp, vp, i, ctypes.c_float, vp]
     L.moe_stats.argtypes = [vp, ctypes.POINTER(Stats)]
     L.moe_reset_stats.argtypes = [vp]
@@ -74,7 +75,7 @@ def lib():
     for name in ("moe_create", "moe_register_router", "moe_register_expert", "moe_forward",
                  "moe_get_routing", "moe_residual_rmsnorm", "moe_stats", "moe_reset_stats",
                  "moe_destroy", "moe_debug_fail_copies", "moe_debug_wait_timeout",
-                 "moe_profile", "moe_profile_read", "moe_forward_residual"):
+                 "moe_profile", "moe_profile_read", "moe_forward_residual", "moe_route_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -106,6 +107,14 @@ def _stream(stream):
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def route_noalloc(x_bf16, W, T, H, E, k, router, idx, w, stream=None):
+    """Routing without allocation (moe_route_noalloc): x bf16 [T,H], W fp32 [E,H] and the
+    outputs idx int32 [T,k], w fp32 [T,k] are device tensors.  Raises MoeError."""
+    st = lib().moe_route_noalloc(_ptr(x_bf16), _ptr(W), T, H, E, k, router, _ptr(idx), _ptr(w), _stream(stream))
+    if st != OK:
+        raise MoeError(st, "moe_route_noalloc")
 
 
 class Context:

@@ -174,6 +174,24 @@ def build_context(cfg, device, max_tokens):
     return ctx
 
 
+def measure_link_gbs(device):
+    """Host -> device bandwidth of this machine: a pinned 1 GiB cudaMemcpyAsync, best of 10."""
+    import torch
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device="cuda:%d" % device)
+    best = 0.0
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, n / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del h, d
+    return best
+
+
 def gateup_bytes_per_expert(cfg):
     H, F = cfg["H"], cfg["F"]
     if cfg["wfmt"] == S.INT4:
@@ -406,8 +424,17 @@ def run_gpu(args, cfg, rank, world, device):
         "wall_s": round(wall, 3),
     }
     if streamed:
+        link = measure_link_gbs(device)
+        miss_gbs = st["bytes_h2d"] / max(1e-9, st["h2d_ms"] / 1e3) / 1e9 if st["h2d_ms"] else None
         out["hit_series_per64"] = hit_series
-        out["h2d_gbs"] = round(st["bytes_h2d"] / max(1e-9, st["h2d_ms"] / 1e3) / 1e9, 2) if st["h2d_ms"] else None
+        out["streaming"] = {
+            "misses_per_token": round(st["misses"] / max(1, K), 2), "hits": st["hits"], "misses": st["misses"],
+            "bytes_h2d": st["bytes_h2d"], "copy_span_ms": round(st["h2d_ms"], 2),
+            "miss_copy_gbs": round(miss_gbs, 2) if miss_gbs else None,
+            "link_gbs_measured": round(link, 2),
+            "miss_frac_of_link": round(miss_gbs / link, 4) if miss_gbs else None,
+            "link_measure": "pinned 1 GiB cudaMemcpyAsync host->device, best of 10, same run",
+            "cache_slots": st["cache_slots"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ctx.close()
         torch.cuda.empty_cache()

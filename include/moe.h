@@ -110,7 +110,8 @@ typedef struct {
     unsigned long long bytes_h2d;             /* expert bytes copied host -> device */
     unsigned long long record_bytes;          /* kernel-layout bytes of one expert */
     unsigned long long cache_slots;           /* HBM expert slots (0 when all resident) */
-    double h2d_ms;                            /* summed wall time of miss copies (streamed) */
+    double h2d_ms;                            /* summed span of the miss copies of each forward,
+                                                 first copy start to last copy end (streamed) */
 } moe_stats_t;
 
 typedef struct moe_ctx moe_ctx;

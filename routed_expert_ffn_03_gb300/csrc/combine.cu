@@ -60,7 +60,9 @@ __global__ void __launch_bounds__(CB_ROWS * CB_KL) combine_kernel(CombineArgs a)
       if (j < a.k) acc = fmaf(a.plan.w[t * a.k + j], y, acc);
       else acc += y;
     }
-    a.out[(size_t)t * a.H + r] = acc;
+    const size_t o = (size_t)t * a.H + r;
+    if (a.xres) a.xres[o] += a.yprev[o];  // stack step: the residual takes y_prev before y is overwritten
+    a.out[o] = acc;
   }
 }
 

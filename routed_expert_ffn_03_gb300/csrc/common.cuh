@@ -122,7 +122,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
@@ -149,11 +149,17 @@ namespace moe {
 // red needs 32 floats.
 __device__ __forceinline__ float block_inv_rms(const float* x, const float* y, int H, float eps, float* red) {
   float ss = 0.f;
-#pragma unroll 4
-  for (int h = threadIdx.x; h < H; h += blockDim.x) {
-    float v = __ldcg(x + h);
-    if (y) v += __ldcg(y + h);
-    ss = fmaf(v, v, ss);
+  const int step = blockDim.x;
+  for (int h0 = threadIdx.x; h0 < H; h0 += 8 * step) {  // 8 (x, y) loads in flight, summed in order
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int h = h0 + q * step;
+      v[q] = h < H ? __ldcg(x + h) : 0.f;
+      if (y && h < H) v[q] += __ldcg(y + h);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);

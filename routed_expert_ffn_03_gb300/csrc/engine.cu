@@ -118,8 +118,12 @@ struct moe_ctx {
   DevCounters* d_counters = nullptr;
   int* h_rb = nullptr;  // pinned readback: hdr(4) | uniq[E] | pass_expert[max_pass]
 
-  cudaStream_t side = nullptr, reg = nullptr;
+  static constexpr int kCopyStreams = 4;
+  cudaStream_t side[kCopyStreams] = {}, reg = nullptr;
   std::vector<cudaEvent_t> copy_ev;
+  cudaEvent_t h2d_t0 = nullptr, h2d_t1[kCopyStreams] = {};
+  bool h2d_pending = false;
+  int h2d_streams_used = 0;
   uint8_t* d_blob_stage = nullptr;
   uint8_t* d_rec_stage = nullptr;
 
@@ -194,8 +198,12 @@ void free_all(moe_ctx* c) {
   cudaFree(c->d_counters);
   if (c->h_rb) cudaFreeHost(c->h_rb);
   for (auto ev : c->copy_ev) cudaEventDestroy(ev);
+  if (c->h2d_t0) cudaEventDestroy(c->h2d_t0);
+  for (auto ev : c->h2d_t1)
+    if (ev) cudaEventDestroy(ev);
   for (auto ev : c->prof_ev) cudaEventDestroy(ev);
-  if (c->side) cudaStreamDestroy(c->side);
+  for (auto st : c->side)
+    if (st) cudaStreamDestroy(st);
   if (c->reg) cudaStreamDestroy(c->reg);
   cudaFree(c->d_blob_stage);
   cudaFree(c->d_rec_stage);
@@ -366,6 +374,8 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     c->slot_pinned.assign(c->n_slots, 0);
     c->copy_ev.resize(E);
     for (auto& ev : c->copy_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    cudaEventCreate(&c->h2d_t0);
+    for (auto& ev : c->h2d_t1) cudaEventCreate(&ev);
   }
   if (cudaHostAlloc((void**)&c->h_rb, (size_t)(8 + E + c->max_pass) * sizeof(int),
                     cudaHostAllocDefault) != cudaSuccess) {
@@ -411,8 +421,9 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   cudaMemset(c->d_status, 0, 4);
   cudaMemset(c->d_counters, 0, sizeof(DevCounters));
   cudaMemset(c->d_plan_mem, 0, 16 * sizeof(int));
-  if (cudaStreamCreateWithFlags(&c->reg, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
+  bool streams_ok = cudaStreamCreateWithFlags(&c->reg, cudaStreamNonBlocking) == cudaSuccess;
+  for (auto& st : c->side) streams_ok = streams_ok && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
+  if (!streams_ok ||
       router_set_attributes() != cudaSuccess || int4_set_attributes(H, maxT) != cudaSuccess ||
       rvq_set_attributes() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
@@ -569,7 +580,6 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   ra.x = (const uint16_t*)x;
   ra.xres = xres;
   ra.yprev = yprev;
-  ra.xres_out = xres;
   ra.xn_out = xn_out;
   ra.eps = eps;
   if (xres) x = xn_out;  // the expert kernels read the normalised input
@@ -601,6 +611,8 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   ca.nks_d = c->rg.m[2].nks;
   ca.has_shared = c->has_shared;
   ca.out = out;
+  ca.xres = (xres && yprev) ? xres : nullptr;
+  ca.yprev = yprev;
 
   if (!c->streamed) {
     ExpertArgs a = expert_args(c, c->d_rec_table + (size_t)layer * (E + 1), x, T);
@@ -640,6 +652,16 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
       return c->sticky;
     }
   }
+  if (c->h2d_pending) {  // the previous forward's copies are complete: add their span
+    float span = 0.f;
+    for (int q = 0; q < c->h2d_streams_used; ++q) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, c->h2d_t0, c->h2d_t1[q]) == cudaSuccess && ms > span) span = ms;
+      cudaGetLastError();
+    }
+    c->h2d_ms += span;
+    c->h2d_pending = false;
+  }
   const int n_pass = rb[0], n_uniq = rb[1], n_routed = rb[2];
   const int* uniq = rb + 8;
   const int* pexp = rb + 8 + E;
@@ -664,9 +686,14 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   }
   c->h_table[E] = c->has_shared ? c->d_shared + (size_t)layer * c->rec_bytes : nullptr;
 
-  // miss copies on the side stream, in ascending expert id, one event each
-  auto t_copy0 = std::chrono::steady_clock::now();
+  // miss copies on the side streams (round-robin), in ascending expert id, one event each
+  const int ns = (int)std::min<size_t>(moe_ctx::kCopyStreams, std::max<size_t>(1, miss_experts.size()));
+  if (!miss_experts.empty()) {
+    CK(cudaEventRecord(c->h2d_t0, c->side[0]));
+    for (int q = 1; q < ns; ++q) CK(cudaStreamWaitEvent(c->side[q], c->h2d_t0, 0));
+  }
   for (size_t m = 0; m < miss_experts.size(); ++m) {
+    cudaStream_t cs = c->side[m % ns];
     const int e = miss_experts[m];
     const uint8_t* src = c->h_pool + ((size_t)layer * E + e) * c->rec_bytes;
     cudaError_t ce;
@@ -674,7 +701,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
       --c->fail_copies;
       ce = cudaErrorInvalidValue;  // injected failure of the copy call
     } else {
-      ce = cudaMemcpyAsync(c->h_table[e], src, c->rec_bytes, cudaMemcpyHostToDevice, c->side);
+      ce = cudaMemcpyAsync(c->h_table[e], src, c->rec_bytes, cudaMemcpyHostToDevice, cs);
     }
     if (ce != cudaSuccess) {
       // the slot's content is unknown now: forget it
@@ -686,8 +713,13 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
         }
       return cuda_fail(c);
     }
-    CK(cudaEventRecord(c->copy_ev[m], c->side));
+    CK(cudaEventRecord(c->copy_ev[m], cs));
     c->bytes_h2d += c->rec_bytes;
+  }
+  if (!miss_experts.empty()) {
+    for (int q = 0; q < ns; ++q) CK(cudaEventRecord(c->h2d_t1[q], c->side[q]));
+    c->h2d_streams_used = ns;
+    c->h2d_pending = true;
   }
 
   // pass order: hits (and the shared expert) first, then each miss's passes
@@ -722,11 +754,6 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     CK(launch_experts(c, a, s));
   }
   CK(launch_combine(ca, s));
-  if (!miss_experts.empty()) {
-    // wall time of the copies as seen by the host (the side stream is otherwise idle)
-    CK(cudaEventSynchronize(c->copy_ev[miss_experts.size() - 1]));
-    c->h2d_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_copy0).count();
-  }
   c->last_T[layer] = T;
   return MOE_OK;
 }
@@ -787,6 +814,16 @@ moe_status moe_stats(moe_ctx* c, moe_stats_t* out) {
   moe_status st = check_device(c);
   DevCounters dc{};
   if (cudaMemcpy(&dc, c->d_counters, sizeof(dc), cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_fail(c);
+  if (c->h2d_pending && st == MOE_OK) {
+    float span = 0.f;
+    for (int q = 0; q < c->h2d_streams_used; ++q) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, c->h2d_t0, c->h2d_t1[q]) == cudaSuccess && ms > span) span = ms;
+      cudaGetLastError();
+    }
+    c->h2d_ms += span;
+    c->h2d_pending = false;
+  }
   memset(out, 0, sizeof(*out));
   out->forwards = dc.forwards;
   out->tokens = dc.tokens;

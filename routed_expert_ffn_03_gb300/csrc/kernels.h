@@ -25,7 +25,6 @@ struct RouterArgs {
   const uint16_t* x;     // bf16 [T][H] router input (when xres is null)
   const float* xres;     // fused stack step: fp32 residual [T][H] (null: not fused)
   const float* yprev;    //   previous layer's output [T][H] or null
-  float* xres_out;       //   x + yprev written here by the last block
   uint16_t* xn_out;      //   bf16(rmsnorm(x + yprev)) written here by the last block
   float eps;
   const float* W;        // [E][H]
@@ -73,6 +72,8 @@ struct CombineArgs {
   const float* part_d;
   int T, H, k, pmax, nks_d, has_shared;
   float* out;
+  float* xres;           // fused stack step: x += yprev here (null: plain forward)
+  const float* yprev;
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 

@@ -8,9 +8,10 @@
 // fp32 logits; equal logits rank the lower expert id first.
 //
 // Optional fused stack step (x, y_prev given): every block computes the token's inverse
-// RMS of x + y_prev with the same fixed-order reduction as the residual_rmsnorm kernel and
-// uses xn = bf16((x + y_prev) * inv) as the router input; the last block, once every block
-// has read x, writes x + y_prev back to x and xn out for the expert kernels.
+// RMS of x + y_prev with the same fixed-order reduction as the residual_rmsnorm kernel,
+// uses xn = bf16((x + y_prev) * inv) as the router input and writes its slice of xn for
+// the expert kernels; the residual x += y_prev is written later by the combine kernel,
+// which reads y_prev just before it overwrites y.
 // Phase 1 (all blocks): each warp owns (expert e, 512-wide chunk c of H) and writes the
 // partial dot products of all T tokens.  Phase 2 (the block that arrives last, found
 // with an atomic ticket; no block waits on another): sums the partials in chunk order
@@ -140,10 +141,6 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
   int* s_idx = s_off + E;                       // [T*k]
   int* s_pos = s_idx + T * k;                   // [T*k]
 
-  if (fused && a.yprev) {
-    // every block has read x: now the residual is updated
-    for (int i = threadIdx.x; i < T * a.H; i += blockDim.x) a.xres_out[i] = a.xres[i] + a.yprev[i];
-  }
 
   // ---------------- phase 2a: logits (all (t, e) in parallel), then top-k per token
   const int tc = max(1, min(T, LOGIT_SMEM / E));
@@ -303,7 +300,7 @@ cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s) {
   const int nch = router_nch(a.H);
   const int nitems = a.E * nch;
   int grid = cdiv(nitems, 8);
-  grid = std::max(1, std::min(grid, 4 * num_sms));
+  grid = std::max(1, std::min(grid, num_sms));
   const size_t smem = (size_t)(LOGIT_SMEM + 2 * a.E + 2 * a.T * a.k) * sizeof(int);
   return launch_pdl(router_kernel, grid, 256, smem, s, a);
 }

@@ -19,24 +19,66 @@
 // q = l XOR i (i = 0..63); the table is laid out [s][c][q] with 64 words per (s, c), so
 // the bank of a lookup is q mod 32 and the 32 lanes hit 32 different banks whatever
 // their codes.  The codes are read with 16-byte streaming loads straight into registers
-// (one task = 32 rows x 64 groups = 6144 contiguous bytes), the next task's loads in
-// flight while the current one is summed.
+// (one task = 32 rows x 64 groups = 6144 contiguous bytes), taken in two halves of 32
+// groups so that the next half is always in flight while the current one is summed;
+// 16 warps per block.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
-constexpr int RV_NW = 8;                               // warps per block
+constexpr int RV_NW = 16;                              // warps per block
 constexpr int RV_LUT_BYTES = 3 * 256 * RVQ_KS * 4;     // 196608
 constexpr int RV_VIN_BYTES = RVQ_KS * RVQ_GROUP * 4;   // 2048
 constexpr int RV_SMEM = RV_LUT_BYTES + RV_VIN_BYTES;
-constexpr int RV_WQ = RVQ_TASK_BYTES / 512;            // 12 uint4 per lane per task
+constexpr int RV_HQ = RVQ_TASK_BYTES / 512 / 2;        // 6 uint4 per lane per half task (32 groups)
 
+// A table entry at byte offset addr + OFF of the table (an ordinary shared-memory load,
+// so it stays ordered after the barrier that ends the table build).
 template <int OFF>
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(addr), "n"(OFF));
-  return v;
+__device__ __forceinline__ float lds_f32(const float* lut, uint32_t addr) {
+  return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(lut) + addr + OFF);
+}
+
+// Half HALF (groups 32 HALF .. 32 HALF + 31 of the lane stream) of a task's codes.
+template <int HALF>
+__device__ __forceinline__ void load_half(uint4 (&v)[RV_HQ], const uint8_t* task, int lane) {
+#pragma unroll
+  for (int j = 0; j < RV_HQ; ++j) v[j] = ldg_stream(task + ((HALF * RV_HQ + j) * 32 + lane) * 16);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 (&v)[RV_HQ], int w) {
+  const uint4& q = v[w >> 2];
+  return (w & 3) == 0 ? q.x : (w & 3) == 1 ? q.y : (w & 3) == 2 ? q.z : q.w;
+}
+
+// Adds the three lookups of each of the half's 32 groups (positions i = 32 HALF + 0..31,
+// group q = lane XOR i) to the stage accumulators.
+template <int HALF>
+__device__ __forceinline__ void rvq_half_sum(const uint4 (&v)[RV_HQ], const float* lut, uint32_t l4, float& acc0,
+                                             float& acc1, float& acc2) {
+#pragma unroll
+  for (int c4 = 0; c4 < 8; ++c4) {
+    const uint32_t w0 = word_of(v, 3 * c4), w1 = word_of(v, 3 * c4 + 1), w2 = word_of(v, 3 * c4 + 2);
+    const int i0 = 32 * HALF + 4 * c4;
+    const uint32_t q0 = l4 ^ (uint32_t)((i0 + 0) << 2);
+    const uint32_t q1 = l4 ^ (uint32_t)((i0 + 1) << 2);
+    const uint32_t q2 = l4 ^ (uint32_t)((i0 + 2) << 2);
+    const uint32_t q3 = l4 ^ (uint32_t)((i0 + 3) << 2);
+    // prmt: byte 1 <- code byte, byte 0 <- qoff, bytes 2,3 <- 0  => (c << 8) | 4q
+    acc0 += lds_f32<0>(lut, prmt(w0, q0, 0x5504));
+    acc1 += lds_f32<65536>(lut, prmt(w0, q0, 0x5514));
+    acc2 += lds_f32<131072>(lut, prmt(w0, q0, 0x5524));
+    acc0 += lds_f32<0>(lut, prmt(w0, q1, 0x5534));
+    acc1 += lds_f32<65536>(lut, prmt(w1, q1, 0x5504));
+    acc2 += lds_f32<131072>(lut, prmt(w1, q1, 0x5514));
+    acc0 += lds_f32<0>(lut, prmt(w1, q2, 0x5524));
+    acc1 += lds_f32<65536>(lut, prmt(w1, q2, 0x5534));
+    acc2 += lds_f32<131072>(lut, prmt(w2, q2, 0x5504));
+    acc0 += lds_f32<0>(lut, prmt(w2, q3, 0x5514));
+    acc1 += lds_f32<65536>(lut, prmt(w2, q3, 0x5524));
+    acc2 += lds_f32<131072>(lut, prmt(w2, q3, 0x5534));
+  }
 }
 
 struct RvUnit {
@@ -45,56 +87,17 @@ struct RvUnit {
 };
 
 template <bool DOWN>
-__device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, long long u, int nks, int p_begin,
-                                          const RecGeom& rg) {
+__device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, int p_begin, const RecGeom& rg) {
   constexpr int mats = DOWN ? 1 : 2;
   RvUnit U;
-  U.ks = (int)(u % nks);
-  const long long pm = u / nks;
-  U.m = (int)(pm % mats);
-  const int pi = (int)(pm / mats);
-  U.pass = a.range.order ? a.range.order[p_begin + pi] : p_begin + pi;
-  U.expert = a.plan.pass_expert[U.pass];
+  U.ks = u % nks;
+  const int pm = u / nks;
+  U.m = pm % mats;
+  const int pi = pm / mats;
+  U.pass = a.range.order ? __ldcg(a.range.order + p_begin + pi) : p_begin + pi;
+  U.expert = __ldcg(a.plan.pass_expert + U.pass);
   U.base = a.rec_table[U.expert] + (DOWN ? rg.off[2] : (U.m == 0 ? rg.off[0] : rg.off[1]));
   return U;
-}
-
-__device__ __forceinline__ void load_task(uint4 (&v)[RV_WQ], const uint8_t* p, int lane) {
-#pragma unroll
-  for (int j = 0; j < RV_WQ; ++j) v[j] = ldg_stream(p + (j * 32 + lane) * 16);
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4 (&v)[RV_WQ], int w) {
-  const uint4& q = v[w >> 2];
-  return (w & 3) == 0 ? q.x : (w & 3) == 1 ? q.y : (w & 3) == 2 ? q.z : q.w;
-}
-
-// Sum of the 64 groups' three lookups for this lane's row.
-__device__ __forceinline__ float rvq_row_sum(const uint4 (&v)[RV_WQ], uint32_t lut, uint32_t l4) {
-  float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f;
-#pragma unroll
-  for (int c4 = 0; c4 < 16; ++c4) {
-    const uint32_t w0 = word_of(v, 3 * c4), w1 = word_of(v, 3 * c4 + 1), w2 = word_of(v, 3 * c4 + 2);
-    // group positions i = 4 c4 + u; code bytes (stage 0,1,2) at stream bytes 3i..3i+2
-    const uint32_t q0 = l4 ^ (uint32_t)((4 * c4 + 0) << 2);
-    const uint32_t q1 = l4 ^ (uint32_t)((4 * c4 + 1) << 2);
-    const uint32_t q2 = l4 ^ (uint32_t)((4 * c4 + 2) << 2);
-    const uint32_t q3 = l4 ^ (uint32_t)((4 * c4 + 3) << 2);
-    // prmt: byte 1 <- code byte, byte 0 <- qoff, bytes 2,3 <- 0  => (c << 8) | 4q
-    acc0 += lds_f32<0>(lut + prmt(w0, q0, 0x5504));
-    acc1 += lds_f32<65536>(lut + prmt(w0, q0, 0x5514));
-    acc2 += lds_f32<131072>(lut + prmt(w0, q0, 0x5524));
-    acc0 += lds_f32<0>(lut + prmt(w0, q1, 0x5534));
-    acc1 += lds_f32<65536>(lut + prmt(w1, q1, 0x5504));
-    acc2 += lds_f32<131072>(lut + prmt(w1, q1, 0x5514));
-    acc0 += lds_f32<0>(lut + prmt(w1, q2, 0x5524));
-    acc1 += lds_f32<65536>(lut + prmt(w1, q2, 0x5534));
-    acc2 += lds_f32<131072>(lut + prmt(w2, q2, 0x5504));
-    acc0 += lds_f32<0>(lut + prmt(w2, q3, 0x5514));
-    acc1 += lds_f32<65536>(lut + prmt(w2, q3, 0x5524));
-    acc2 += lds_f32<131072>(lut + prmt(w2, q3, 0x5534));
-  }
-  return (acc0 + acc1) + acc2;
 }
 
 template <bool DOWN>
@@ -102,7 +105,7 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   float* lutf = reinterpret_cast<float*>(smem);
   float* vin = reinterpret_cast<float*>(smem + RV_LUT_BYTES);
-  const uint32_t lut = smem_u32(smem);
+  constexpr int nthr = RV_NW * 32;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, p = lane & 3;
@@ -113,28 +116,29 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   const int nks = g.nks, ntask = g.ntask;
   const int rows32 = ntask * 32, rows32_gu = gg.ntask * 32;
   const int p_begin = a.range.p_begin;
-  const int p_end = a.range.p_end < 0 ? a.plan.hdr->n_pass : a.range.p_end;
-  const long long total = (long long)max(0, p_end - p_begin) * mats * nks * ntask;
-  const long long t0 = total * blockIdx.x / gridDim.x;
-  const long long t1 = total * (blockIdx.x + 1) / gridDim.x;
+  const int p_end = a.range.p_end < 0 ? __ldcg(&a.plan.hdr->n_pass) : a.range.p_end;
+  const int total = max(0, p_end - p_begin) * mats * nks * ntask;
+  const int t0 = (int)((long long)total * blockIdx.x / gridDim.x);
+  const int t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
   const uint32_t l4 = (uint32_t)lane << 2;
 
-  for (long long i = t0; i < t1;) {
-    const long long u = i / ntask;
-    const long long seg_end = min(t1, (u + 1) * ntask);
+  for (int i = t0; i < t1;) {
+    const int u = i / ntask;
+    const int seg_end = min(t1, (u + 1) * ntask);
     const RvUnit U = rv_unit<DOWN>(a, u, nks, p_begin, rg);
     const uint8_t* codes = U.base + RVQ_CB_BYTES + (size_t)U.ks * ntask * RVQ_TASK_BYTES;
+    const int useg = u * ntask;
 
-    // first task's codes go in flight before the table is built
-    long long ti = i + warp;
-    uint4 va[RV_WQ], vb[RV_WQ];
-    if (ti < seg_end) load_task(va, codes + (size_t)(ti % ntask) * RVQ_TASK_BYTES, lane);
+    // first half of this warp's first task goes in flight before the table is built
+    int ti = i + warp;
+    uint4 ha[RV_HQ], hb[RV_HQ];
+    if (ti < seg_end) load_half<0>(ha, codes + (size_t)(ti - useg) * RVQ_TASK_BYTES, lane);
 
     __syncthreads();  // the previous unit's table is no longer read
     {
-      const int tok = a.plan.pass_tok[U.pass];   // one token per pass
+      const int tok = __ldcg(a.plan.pass_tok + U.pass);   // one token per pass
       const int kbase = U.ks * RVQ_KS * RVQ_GROUP;
-      for (int e = threadIdx.x; e < RVQ_KS * RVQ_GROUP; e += RV_NW * 32) {
+      for (int e = threadIdx.x; e < RVQ_KS * RVQ_GROUP; e += nthr) {
         const int k = kbase + e;
         float v = 0.f;
         if (k < g.K) {
@@ -144,10 +148,19 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
             const float* pg = a.part_gu + ((size_t)(U.pass * 2 + 0) * gg.nks) * rows32_gu + k;
             const float* pu = a.part_gu + ((size_t)(U.pass * 2 + 1) * gg.nks) * rows32_gu + k;
             float gs = 0.f, us = 0.f;
-#pragma unroll 4
-            for (int s2 = 0; s2 < gg.nks; ++s2) {
-              gs += __ldcg(pg + (size_t)s2 * rows32_gu);
-              us += __ldcg(pu + (size_t)s2 * rows32_gu);
+            for (int s0 = 0; s0 < gg.nks; s0 += 8) {  // 16 loads in flight, added in slice order
+              float gv[8], uv[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const bool in = s0 + q < gg.nks;
+                gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * rows32_gu) : 0.f;
+                uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * rows32_gu) : 0.f;
+              }
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                gs += gv[q];
+                us += uv[q];
+              }
             }
             v = gs / (1.f + expf(-gs)) * us;
           }
@@ -198,26 +211,19 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
     }
     __syncthreads();
 
-    // tasks of this unit: warp-strided, two register buffers
-    const size_t out_base = DOWN ? ((size_t)U.pass * nks + U.ks) * rows32
-                                 : ((size_t)(U.pass * 2 + U.m) * nks + U.ks) * rows32;
-    float* outp = DOWN ? a.part_d : a.part_gu;
+    // tasks of this unit: warp-strided; half tasks double-buffered in registers
+    float* outp = (DOWN ? a.part_d + ((size_t)U.pass * nks + U.ks) * rows32
+                        : a.part_gu + ((size_t)(U.pass * 2 + U.m) * nks + U.ks) * rows32);
     while (ti < seg_end) {
-      const long long tn = ti + RV_NW;
-      if (tn < seg_end) load_task(vb, codes + (size_t)(tn % ntask) * RVQ_TASK_BYTES, lane);
-      {
-        const float y = rvq_row_sum(va, lut, l4);
-        outp[out_base + (size_t)(ti % ntask) * 32 + lane] = y;
-      }
+      const uint8_t* task = codes + (size_t)(ti - useg) * RVQ_TASK_BYTES;
+      load_half<1>(hb, task, lane);
+      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f;
+      rvq_half_sum<0>(ha, lutf, l4, acc0, acc1, acc2);
+      const int tn = ti + RV_NW;
+      if (tn < seg_end) load_half<0>(ha, codes + (size_t)(tn - useg) * RVQ_TASK_BYTES, lane);
+      rvq_half_sum<1>(hb, lutf, l4, acc0, acc1, acc2);
+      outp[(size_t)(ti - useg) * 32 + lane] = (acc0 + acc1) + acc2;
       ti = tn;
-      if (ti >= seg_end) break;
-      const long long tn2 = ti + RV_NW;
-      if (tn2 < seg_end) load_task(va, codes + (size_t)(tn2 % ntask) * RVQ_TASK_BYTES, lane);
-      {
-        const float y = rvq_row_sum(vb, lut, l4);
-        outp[out_base + (size_t)(ti % ntask) * 32 + lane] = y;
-      }
-      ti = tn2;
     }
     i = seg_end;
   }

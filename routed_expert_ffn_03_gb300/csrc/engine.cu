@@ -113,6 +113,7 @@ struct moe_ctx {
   float* d_h = nullptr;        // int4 SwiGLU outputs
   float* d_part_d = nullptr;
   int max_pass = 0;
+  int big_min = 0, max_big = 0;      // dense (tcgen05) groups: RVQ, resident, max_tokens >= 8
   uint32_t* d_status = nullptr;
   uint32_t* d_dbg_status = nullptr;
   DevCounters* d_counters = nullptr;
@@ -296,8 +297,12 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const MatGeom& gg = c->rg.m[0];
   const MatGeom& gd = c->rg.m[2];
   const bool int4 = cfg->wfmt == MOE_W_INT4_G128;
+  if (!int4 && !c->streamed && maxT >= GEMM_MIN_TOKENS) {
+    c->big_min = GEMM_MIN_TOKENS;
+    c->max_big = c->max_pass / GEMM_MIN_TOKENS + 2;
+  }
   const size_t part_gu = (size_t)c->max_pass * 2 * gg.nks * gg.ntask * 32 * c->pmax;
-  const size_t hbuf = int4 ? (size_t)c->max_pass * c->pmax * gg.ntask * 32 : 0;
+  const size_t hbuf = (int4 || c->big_min) ? (size_t)c->max_pass * c->pmax * gg.ntask * 32 : 0;
   const size_t part_d = (size_t)c->max_pass * gd.nks * gd.ntask * 32 * c->pmax;
   const size_t rpart = (size_t)E * router_nch(H) * maxT;
   const size_t router_bytes = (size_t)L * E * H * sizeof(float);
@@ -400,7 +405,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   {
     // plan arrays, one allocation
     const size_t n_int = 16 + (size_t)c->max_pass * (2 + c->pmax) + (size_t)maxT * k * 4 +
-                         (size_t)maxT * 2 + E;
+                         (size_t)maxT * 2 + E + (size_t)c->max_big * 3 + c->max_pass;
     AL(c->d_plan_mem, n_int * sizeof(int));
     int* p = (int*)c->d_plan_mem;
     c->plan.hdr = (Plan*)p;
@@ -415,6 +420,8 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     c->plan.shared_pass = p; p += maxT;
     c->plan.shared_slot = p; p += maxT;
     c->plan.uniq = p; p += E;
+    c->plan.big = p; p += (size_t)c->max_big * 3;
+    c->plan.small_order = p; p += c->max_pass;
   }
 #undef AL
   cudaMemset(c->d_ticket, 0, sizeof(unsigned int));
@@ -425,7 +432,8 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   for (auto& st : c->side) streams_ok = streams_ok && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
   if (!streams_ok ||
       router_set_attributes() != cudaSuccess || int4_set_attributes(H, maxT) != cudaSuccess ||
-      rvq_set_attributes() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      rvq_set_attributes() != cudaSuccess || rvq_gemm_set_attributes() != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     free_all(c);
     delete c;
@@ -517,6 +525,7 @@ static ExpertArgs expert_args(moe_ctx* c, uint8_t* const* table, const void* x, 
   a.range.order = nullptr;
   a.range.p_begin = 0;
   a.range.p_end = -1;
+  a.range.count = nullptr;
   a.status = c->d_status;
   a.budget = c->budget;
   return a;
@@ -598,6 +607,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   ra.store_w = c->d_store_w + (size_t)layer * c->cfg.max_tokens * k;
   ra.counters = c->d_counters;
   ra.record_bytes = c->rec_bytes;
+  ra.big_min = c->big_min;
   if (c->prof && !c->streamed) CK(cudaEventRecordWithFlags(c->prof_ev[(size_t)layer * 5], s, cudaEventRecordExternal));
   CK(launch_router(ra, c->num_sms, s));
 
@@ -622,6 +632,16 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
       CK(launch_int4_gateup(a, c->num_sms, s));
       if (ev) CK(cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal));
       CK(launch_int4_down(a, c->num_sms, s));
+    } else if (c->big_min > 0) {
+      // per-token path over the small passes, tcgen05 path over the dense groups
+      ExpertArgs as = a;
+      as.range.order = c->plan.small_order;
+      as.range.count = &c->plan.hdr->n_small;
+      CK(launch_rvq_gateup(as, c->num_sms, s));
+      CK(launch_rvq_gemm_gateup(a, c->num_sms, s));
+      if (ev) CK(cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal));
+      CK(launch_rvq_down(as, c->num_sms, s));
+      CK(launch_rvq_gemm_down(a, c->num_sms, s, c->max_big));
     } else {
       CK(launch_rvq_gateup(a, c->num_sms, s));
       if (ev) CK(cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal));

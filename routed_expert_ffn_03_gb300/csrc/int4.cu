@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
 
   pdl_wait();  // the plan and x come from the kernels before
   const int p_begin = a.range.p_begin;
-  const int p_end = a.range.p_end < 0 ? __ldcg(&a.plan.hdr->n_pass) : a.range.p_end;
+  const int p_end = a.range.p_end >= 0 ? a.range.p_end : __ldcg(a.range.count ? a.range.count : &a.plan.hdr->n_pass);
   const int total = max(0, p_end - p_begin) * per_pass;
   const int t0 = (int)((long long)total * blockIdx.x / gridDim.x);
   const int t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
   // The plan is older than the gate/up kernel, which waited for it before it let this
   // kernel start, so the weights stream before the gate/up partials are ready.
   const int p_begin = a.range.p_begin;
-  const int p_end = a.range.p_end < 0 ? __ldcg(&a.plan.hdr->n_pass) : a.range.p_end;
+  const int p_end = a.range.p_end >= 0 ? a.range.p_end : __ldcg(a.range.count ? a.range.count : &a.plan.hdr->n_pass);
   const int total = max(0, p_end - p_begin) * per_pass;
   const int t0 = (int)((long long)total * blockIdx.x / gridDim.x);
   const int t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);

@@ -36,6 +36,7 @@ struct RouterArgs {
   float* store_w;
   DevCounters* counters;
   unsigned long long record_bytes;
+  int big_min;           // > 0: experts with >= big_min tokens form dense groups (pmax must be 1)
 };
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s);
 cudaError_t router_set_attributes();
@@ -46,6 +47,7 @@ int router_nch(int H);
 struct PassRange {
   const int* order;
   int p_begin, p_end;
+  const int* count;   // with p_end < 0: the pass count lives here (null: the plan's n_pass)
 };
 
 struct ExpertArgs {
@@ -54,7 +56,7 @@ struct ExpertArgs {
   int H, F, E, T, max_tokens;
   const uint16_t* x;                // bf16 [T][H] (gate/up input)
   float* part_gu;                   // [max_pass][2][nks_gu][pmax][rows32(F)] gate/up partials
-  float* h;                         // int4: [max_pass][pmax][rows32(F)] SwiGLU outputs
+  float* h;                         // [max_pass][pmax][rows32(F)] SwiGLU outputs (int4; RVQ dense path)
   float* part_d;                    // [max_pass][nks_d][pmax][rows32(H)]
   PassRange range;
   uint32_t* status;
@@ -66,6 +68,9 @@ cudaError_t launch_int4_gateup(const ExpertArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_int4_down(const ExpertArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_rvq_gateup(const ExpertArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_rvq_down(const ExpertArgs& a, int grid, cudaStream_t s);
+cudaError_t rvq_gemm_set_attributes();
+cudaError_t launch_rvq_gemm_gateup(const ExpertArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_rvq_gemm_down(const ExpertArgs& a, int grid, cudaStream_t s, int max_big);
 
 struct CombineArgs {
   PlanPtrs plan;

@@ -123,7 +123,12 @@ struct Plan {
   int n_uniq;          // unique routed experts
   int n_routed_pass;   // passes of routed experts (shared passes follow)
   int T;
+  int n_big;           // expert token groups for the dense (tcgen05) path
+  int n_small;         // passes left for the per-token path (listed in small_order)
 };
+
+constexpr int GEMM_MIN_TOKENS = 8;   // an expert with this many tokens takes the dense path
+constexpr int GEMM_MAX_TOKENS = 32;  // tokens per dense group (64 mma columns, hi/lo)
 
 struct PlanPtrs {
   Plan* hdr;
@@ -137,6 +142,8 @@ struct PlanPtrs {
   int* uniq;           // [E]
   int* idx;            // [maxT][k]   routing of this forward
   float* w;            // [maxT][k]
+  int* big;            // [max_big][3] (expert, first pass, tokens) of the dense groups
+  int* small_order;    // [max_pass]   the other passes, ascending
 };
 
 }  // namespace moe

@@ -288,7 +288,37 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
       }
     }
   }
-  if (threadIdx.x == 0) *a.ticket = 0u;  // ready for the next launch (stream-ordered)
+  // dense groups (pmax == 1: one pass per token): experts with >= big_min tokens go to the
+  // tcgen05 path in balanced chunks of <= GEMM_MAX_TOKENS, every other pass to the
+  // per-token path, both lists in ascending expert id then token order
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int nb = 0, ns = 0;
+    auto emit = [&](int expert, int first, int c) {
+      if (a.big_min > 0 && c >= a.big_min) {
+        const int nch = cdiv(c, GEMM_MAX_TOKENS), base = c / nch, rem = c % nch;
+        int start = 0;
+        for (int q = 0; q < nch; ++q) {
+          const int sz = base + (q < rem ? 1 : 0);
+          a.plan.big[3 * nb + 0] = expert;
+          a.plan.big[3 * nb + 1] = first + start;
+          a.plan.big[3 * nb + 2] = sz;
+          ++nb;
+          start += sz;
+        }
+      } else if (a.big_min > 0) {
+        for (int i = 0; i < c; ++i) a.plan.small_order[ns++] = first + i;
+      }
+    };
+    if (a.big_min > 0) {
+      for (int e = 0; e < E; ++e)
+        if (s_cnt[e] > 0) emit(e, s_off[e], s_cnt[e]);
+      if (a.has_shared) emit(E, routed_passes, T);
+    }
+    a.plan.hdr->n_big = nb;
+    a.plan.hdr->n_small = a.big_min > 0 ? ns : routed_passes + (a.has_shared ? cdiv(T, pmax) : 0);
+    *a.ticket = 0u;  // ready for the next launch (stream-ordered)
+  }
 }
 
 cudaError_t router_set_attributes() {

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   const int nks = g.nks, ntask = g.ntask;
   const int rows32 = ntask * 32, rows32_gu = gg.ntask * 32;
   const int p_begin = a.range.p_begin;
-  const int p_end = a.range.p_end < 0 ? __ldcg(&a.plan.hdr->n_pass) : a.range.p_end;
+  const int p_end = a.range.p_end >= 0 ? a.range.p_end : __ldcg(a.range.count ? a.range.count : &a.plan.hdr->n_pass);
   const int total = max(0, p_end - p_begin) * mats * nks * ntask;
   const int t0 = (int)((long long)total * blockIdx.x / gridDim.x);
   const int t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);

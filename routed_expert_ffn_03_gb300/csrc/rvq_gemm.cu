@@ -1,0 +1,361 @@
+// rvq_gemm.cu - tcgen05 grouped GEMM for RVQ experts that serve many tokens at once.
+//
+// When one expert is selected by >= GEMM_MIN tokens of a forward (the always-on shared
+// expert at T = 32, a draft-verify batch, prefill-like T), its weights are worth
+// streaming once and multiplying against all of those tokens as a dense contraction:
+//     Y[r][n] = sum_k W[r][k] X[k][n],   W = W0 + W1 + W2,  W_s[r][8q+i] = C_s[c_s(r,q)][i]
+// Each stage W_s is a gather of stored fp16 codebook rows, so it is exact in fp16; the
+// activations enter as fp16 hi + lo columns (n = 2 token + part), so all products are
+// exact and the three stages and all k accumulate in fp32 in tensor memory.
+//
+// Work item = (group of <= 32 tokens of one expert, matrix, 512-input k-slice, 128-row
+// tile).  A block (8 warps) takes items round-robin.  Per item: one bulk TMA copy each of
+// the matrix's codebooks (12 KB) and the tile's codes (4 row blocks x 6 KB); the B
+// operand (X hi/lo, K-major canonical layout, no swizzle) is built once; then for each of
+// the 8 k-blocks of 64 inputs the block gathers the three A stage tiles (128 x 64 fp16
+// each, K-major canonical layout) into one of two buffers and one thread issues
+// 3 x 4 tcgen05.mma (M = 128, N = 16..64, K = 16) into the TMEM accumulator, committing
+// to that buffer's mbarrier so the gather of the next k-block overlaps them.  The
+// epilogue reads TMEM with tcgen05.ld (warps 0-3, one TMEM lane quarter each) and writes
+// the k-slice partial of every token in the same layout the lookup-table path uses
+// (part_gu[pass][m][ks][row], part_d[pass][ks][row]), so the SwiGLU and combine steps
+// are shared.  Every wait is bounded; the tensor memory is always released.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int GM_TILE_M = 128;
+constexpr int GM_KB = 64;                                   // inputs per k-block
+constexpr int GM_NKB = RVQ_KS * RVQ_GROUP / GM_KB;          // 8 k-blocks per 512-input slice
+constexpr int GM_MAXN = 64;                                 // 32 tokens x hi/lo
+constexpr int GM_CB = RVQ_CB_BYTES;                         // 12288
+constexpr int GM_CODES = 4 * RVQ_TASK_BYTES;                // 24576 (4 row blocks of 32)
+constexpr int GM_B = GM_MAXN * RVQ_KS * RVQ_GROUP * 2;      // 65536: N x 512 fp16
+constexpr int GM_ASTAGE = GM_TILE_M * GM_KB * 2;            // 16384: 128 x 64 fp16
+constexpr int GM_A = 2 * 3 * GM_ASTAGE;                     // two buffers x three stages
+constexpr int GM_OFF_CODES = GM_CB;
+constexpr int GM_OFF_B = GM_OFF_CODES + GM_CODES;
+constexpr int GM_OFF_A = GM_OFF_B + GM_B;
+constexpr int GM_OFF_BAR = GM_OFF_A + GM_A;                 // 3 mbarriers + tmem address
+constexpr int GM_SMEM = GM_OFF_BAR + 64;
+constexpr int GM_THREADS = 256;
+constexpr int GM_TMEM_COLS = 64;
+
+// ---------------------------------------------------------------- tcgen05 helpers
+__device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  // K-major, no swizzle: start >> 4 [0,14), leading (K-direction core matrix) byte offset
+  // >> 4 [16,30), stride (M/N-direction 8-row group) byte offset >> 4 [32,46), descriptor
+  // version 1 [46,48), layout type 0 (no swizzle) [61,64).
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, M, N.
+__host__ __device__ __forceinline__ uint32_t umma_idesc_f16(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Byte offset of element (row, k) in a K-major, no-swizzle canonical tile whose rows are
+// kcores * 8 elements long: core matrix (row / 8, k / 8) of 8 x 8 fp16 (128 B), rows of a
+// core 16 B apart, cores along K 128 B apart, 8-row groups kcores * 128 B apart.
+__device__ __forceinline__ uint32_t canon_off(int row, int k, int kcores) {
+  return (uint32_t)(((row >> 3) * kcores + (k >> 3)) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
+
+struct GmItem {
+  int grp, m, ks, tile;
+};
+
+template <bool DOWN>
+__global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const RecGeom rg = rec_geom(WFMT_RVQ, a.H, a.F);
+  const MatGeom g = rg.m[DOWN ? 2 : 0];
+  const MatGeom gg = rg.m[0];
+  constexpr int mats = DOWN ? 1 : 2;
+  const int nks = g.nks, ntile = cdiv(g.rows, GM_TILE_M);
+  const int rows32 = g.ntask * 32, rows32_gu = gg.ntask * 32;
+
+  uint8_t* cb = smem;
+  uint8_t* codes = smem + GM_OFF_CODES;
+  uint8_t* bsm = smem + GM_OFF_B;
+  uint8_t* asm_ = smem + GM_OFF_A;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GM_OFF_BAR);  // [0] tma, [1..2] mma buffers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM_OFF_BAR + 32);
+  __shared__ volatile int s_abort;
+  const uint32_t bar_tma = smem_u32(bars), bar_mma0 = smem_u32(bars + 1);
+
+  const int n_big = __ldcg(&a.plan.hdr->n_big);
+  const int total = n_big * mats * nks * ntile;
+  if (blockIdx.x >= total) return;  // uniform across the block: no tensor memory taken
+
+  if (tid == 0) {
+    mbar_init(bar_tma, 1);
+    mbar_init(bar_mma0, 1);
+    mbar_init(bar_mma0 + 8, 1);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(GM_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int tma_phase = 0, mma_phase[2] = {0, 0}, mma_pending[2] = {0, 0};
+  for (int it = blockIdx.x; it < total && !s_abort; it += gridDim.x) {
+    GmItem I;
+    I.tile = it % ntile;
+    int rest = it / ntile;
+    I.ks = rest % nks;
+    rest /= nks;
+    I.m = rest % mats;
+    I.grp = rest / mats;
+    const int expert = __ldcg(a.plan.big + 3 * I.grp + 0);
+    const int pass0 = __ldcg(a.plan.big + 3 * I.grp + 1);
+    const int ntok = __ldcg(a.plan.big + 3 * I.grp + 2);
+    const int N = max(16, (2 * ntok + 15) & ~15);
+    const uint8_t* mat = a.rec_table[expert] + (DOWN ? rg.off[2] : (I.m == 0 ? rg.off[0] : rg.off[1]));
+    const int rb0 = I.tile * 4, nrb = min(4, g.ntask - rb0);
+
+    // codebooks and codes of this tile and slice
+    if (tid == 0) {
+      const uint32_t bytes = GM_CB + nrb * RVQ_TASK_BYTES;
+      fence_async_smem();  // the previous item read these buffers through the generic proxy
+      mbar_arrive_expect_tx(bar_tma, bytes);
+      bulk_g2s(smem_u32(cb), mat, GM_CB, bar_tma);
+      bulk_g2s(smem_u32(codes), mat + GM_CB + ((size_t)I.ks * g.ntask + rb0) * RVQ_TASK_BYTES,
+               nrb * RVQ_TASK_BYTES, bar_tma);
+    }
+    // B operand: column n = 2 t + part of token t of the group, K-major canonical layout
+    const int kbase = I.ks * RVQ_KS * RVQ_GROUP;
+    for (int e = tid; e < N * (RVQ_KS * RVQ_GROUP / 2); e += GM_THREADS) {
+      const int n = e / (RVQ_KS * RVQ_GROUP / 2), kp = e - n * (RVQ_KS * RVQ_GROUP / 2);
+      const int k = 2 * kp;               // two inputs per thread step
+      const int t = n >> 1, part = n & 1;
+      float v0 = 0.f, v1 = 0.f;
+      if (t < ntok) {
+        const int pass = pass0 + t;
+        const int kk0 = kbase + k;
+        if (!DOWN) {
+          const int tok = __ldcg(a.plan.pass_tok + pass);
+          if (kk0 < g.K) v0 = bf16_bits_to_float(a.x[(size_t)tok * a.H + kk0]);
+          if (kk0 + 1 < g.K) v1 = bf16_bits_to_float(a.x[(size_t)tok * a.H + kk0 + 1]);
+        } else {
+          const float* hp = a.h + (size_t)pass * rows32_gu;   // SwiGLU of this pass (rvq_swiglu_big)
+          if (kk0 < g.K) v0 = __ldcg(hp + kk0);
+          if (kk0 + 1 < g.K) v1 = __ldcg(hp + kk0 + 1);
+        }
+      }
+      __half h0, l0, h1, l1;
+      split_half(v0, h0, l0);
+      split_half(v1, h1, l1);
+      const uint32_t pk = part ? pack_half2(l0, l1) : pack_half2(h0, h1);
+      *reinterpret_cast<uint32_t*>(bsm + canon_off(n, k, RVQ_KS * RVQ_GROUP / 8)) = pk;
+    }
+    // the tile's codes must have landed before the gather
+    bool ok = mbar_wait_bounded(bar_tma, tma_phase & 1, a.budget);
+    tma_phase ^= 1;
+    if (!ok) {
+      s_abort = 1;
+      atomicOr(a.status, ST_TIMEOUT);
+    }
+    __syncthreads();
+    if (s_abort) break;
+
+    const uint32_t idesc = umma_idesc_f16(GM_TILE_M, N);
+    for (int kb = 0; kb < GM_NKB; ++kb) {
+      const int buf = kb & 1;
+      uint8_t* abuf = asm_ + buf * 3 * GM_ASTAGE;
+      if (mma_pending[buf]) {  // the mma that read this buffer two k-blocks ago is done
+        ok = mbar_wait_bounded(bar_mma0 + 8 * buf, mma_phase[buf] & 1, a.budget);
+        mma_phase[buf] ^= 1;
+        mma_pending[buf] = 0;
+        if (!ok) {
+          s_abort = 1;
+          atomicOr(a.status, ST_TIMEOUT);
+        }
+        tc_fence_after();
+      }
+      // gather: (row, group of 8 inputs, stage) -> 16 B codebook row into stage tile
+      for (int e = tid; e < GM_TILE_M * 8; e += GM_THREADS) {
+        const int r = e & (GM_TILE_M - 1), gi = e >> 7;  // gi: group within the k-block
+        const int rbl = r >> 5, l = r & 31;
+        const int q = kb * 8 + gi;                        // group within the slice
+        const int i = l ^ q;                              // position in the lane stream
+        const uint8_t* lanebase = codes + rbl * RVQ_TASK_BYTES + l * 16;
+#pragma unroll
+        for (int s = 0; s < 3; ++s) {
+          const int bp = 3 * i + s;                       // stream byte
+          uint32_t code = 0;
+          if (rbl < nrb) code = lanebase[(bp >> 4) * 512 + (bp & 15)];
+          const uint4 v = *reinterpret_cast<const uint4*>(cb + ((s * 256 + code) * 8) * 2);
+          *reinterpret_cast<uint4*>(abuf + s * GM_ASTAGE + canon_off(r, gi * 8, GM_KB / 8)) = v;
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      if (s_abort) break;
+      if (tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 3; ++s) {
+#pragma unroll
+          for (int kk = 0; kk < GM_KB / 16; ++kk) {
+            const uint64_t ad = umma_smem_desc(smem_u32(abuf + s * GM_ASTAGE) + kk * 2 * 128, 128, (GM_KB / 8) * 128);
+            const uint64_t bd = umma_smem_desc(smem_u32(bsm) + (kb * (GM_KB / 8) + kk * 2) * 128, 128,
+                                               (RVQ_KS * RVQ_GROUP / 8) * 128);
+            tc_mma(tmem, ad, bd, idesc, kb > 0 || s > 0 || kk > 0);
+          }
+        }
+        tc_commit(bar_mma0 + 8 * buf);
+      }
+      mma_pending[buf] = 1;
+    }
+    if (s_abort) break;
+    // all mma of this item done (the last commit covers every earlier one)
+    const int lastbuf = (GM_NKB - 1) & 1;
+    ok = mbar_wait_bounded(bar_mma0 + 8 * lastbuf, mma_phase[lastbuf] & 1, a.budget);
+    mma_phase[lastbuf] ^= 1;
+    mma_pending[lastbuf] = 0;
+    if (mma_pending[lastbuf ^ 1]) {  // its phase also completed (earlier commit)
+      ok = ok && mbar_wait_bounded(bar_mma0 + 8 * (lastbuf ^ 1), mma_phase[lastbuf ^ 1] & 1, a.budget);
+      mma_phase[lastbuf ^ 1] ^= 1;
+      mma_pending[lastbuf ^ 1] = 0;
+    }
+    if (!ok) {
+      s_abort = 1;
+      atomicOr(a.status, ST_TIMEOUT);
+    }
+    __syncthreads();  // the abort flag is the same for every thread from here
+    tc_fence_after();
+    if (warp < 4 && !s_abort) {
+      const int r = warp * 32 + lane;                 // TMEM lane = tile row
+      const int row = I.tile * GM_TILE_M + r;
+      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16];
+        tc_ld16(taddr + c0, v);
+        if (row < g.rows) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int t = (c0 >> 1) + q;
+            if (t < ntok) {
+              const int pass = pass0 + t;
+              float* dst = DOWN ? a.part_d + ((size_t)pass * nks + I.ks) * rows32
+                                : a.part_gu + ((size_t)(pass * 2 + I.m) * nks + I.ks) * rows32;
+              dst[row] = v[2 * q] + v[2 * q + 1];
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // TMEM read and smem reused by the next item
+  }
+  // release: every issued mma has completed (bounded), then the tensor memory
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b)
+      if (mma_pending[b] && !mbar_wait_bounded(bar_mma0 + 8 * b, mma_phase[b] & 1, a.budget))
+        atomicOr(a.status, ST_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(GM_TMEM_COLS) : "memory");
+}
+
+// h[pass][row] = silu(g) * u for the passes of the GEMM groups, g and u the gate / up
+// k-slice partials added in slice order (the same order the lookup-table down kernel uses).
+__global__ void __launch_bounds__(256) rvq_swiglu_big_kernel(ExpertArgs a) {
+  const RecGeom rg = rec_geom(WFMT_RVQ, a.H, a.F);
+  const MatGeom gg = rg.m[0];
+  const int rows32 = gg.ntask * 32;
+  const int grp = blockIdx.y;
+  if (grp >= __ldcg(&a.plan.hdr->n_big)) return;
+  const int pass0 = __ldcg(a.plan.big + 3 * grp + 1), ntok = __ldcg(a.plan.big + 3 * grp + 2);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ntok * a.F; i += gridDim.x * blockDim.x) {
+    const int t = i / a.F, r = i - t * a.F;
+    const int pass = pass0 + t;
+    const float* pg = a.part_gu + ((size_t)(pass * 2 + 0) * gg.nks) * rows32 + r;
+    const float* pu = a.part_gu + ((size_t)(pass * 2 + 1) * gg.nks) * rows32 + r;
+    float gs = 0.f, us = 0.f;
+    for (int s0 = 0; s0 < gg.nks; s0 += 8) {
+      float gv[8], uv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const bool in = s0 + q < gg.nks;
+        gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * rows32) : 0.f;
+        uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * rows32) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        gs += gv[q];
+        us += uv[q];
+      }
+    }
+    a.h[(size_t)pass * rows32 + r] = gs / (1.f + expf(-gs)) * us;
+  }
+}
+
+cudaError_t rvq_gemm_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(rvq_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(rvq_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+}
+
+cudaError_t launch_rvq_gemm_gateup(const ExpertArgs& a, int grid, cudaStream_t s) {
+  rvq_gemm_kernel<false><<<grid, GM_THREADS, GM_SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+cudaError_t launch_rvq_gemm_down(const ExpertArgs& a, int grid, cudaStream_t s, int max_big) {
+  dim3 sg(cdiv(a.F, 256), max_big);
+  rvq_swiglu_big_kernel<<<sg, 256, 0, s>>>(a);
+  rvq_gemm_kernel<true><<<grid, GM_THREADS, GM_SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -28,7 +28,7 @@ def _register_device(spec, max_tokens):
 
 @pytest.mark.parametrize("name,spec,Ts,trace", [
     ("mixtral", LayerSpec(4096, 14336, 8, 2, S.INT4, router=0, seed=0), (1, 4), "iid"),
-    ("dsv3", LayerSpec(7168, 2048, 256, 8, S.RVQ, router=1, shared=True, seed=0), (1, 4), "iid"),
+    ("dsv3", LayerSpec(7168, 2048, 256, 8, S.RVQ, router=1, shared=True, seed=0), (1, 4, 32), "iid"),
     ("wide", LayerSpec(7168, 1536, 384, 16, S.RVQ, router=0, seed=0), (1,), "domain"),
 ])
 def test_full_layer(name, spec, Ts, trace):

@@ -41,7 +41,9 @@ def test_tiny_config_rvq_top2_softmax():
     (264, 200, 33, 3, 3, 1, True),      # ragged k-slice (33 groups), E > 32, sigmoid + shared
     (520, 96, 7, 7, 4, 0, False),       # k = E
     (128, 64, 300, 8, 2, 1, False),     # E > 256
-    (256, 136, 16, 4, 32, 0, True),     # T = 32 with shared expert
+    (256, 136, 16, 4, 32, 0, True),     # T = 32 with shared expert (dense tcgen05 groups)
+    (512, 384, 4, 2, 16, 1, True),      # T = 16: most experts take the dense path
+    (264, 200, 3, 3, 40, 0, False),     # 40 tokens on every expert: split into 2 dense groups
 ])
 def test_rvq_odd_shapes(H, F, E, k, T, router, shared):
     _run(LayerSpec(H, F, E, k, S.RVQ, router=router, shared=shared, seed=H + F + E), T)

@@ -98,31 +98,31 @@ __device__ __forceinline__ void i4_task(const uint8_t* st, int ng, const uint2* 
     const uint4 wb1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK + 512 + lane * 16);
     const uint32_t sc0 = *reinterpret_cast<const uint32_t*>(blk + 1024 + gq * 4);
     const uint32_t sc1 = *reinterpret_cast<const uint32_t*>(blk + I4_BLOCK + 1024 + gq * 4);
-    // two independent accumulation chains per tile (even / odd k-steps)
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    // lanes whose mma column carries no token read a zero fragment (no branch)
+    const uint2* xg = xf + gi * 8 * nb * 4 + (gq < nb ? lane : 0);
+    const bool live = gq < nb;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      uint2 b = make_uint2(0u, 0u);
-      if (gq < nb) b = xf[(gi * 8 + j) * nb * 4 + lane];
+      uint2 b = xg[j * nb * 4];
+      b.x = live ? b.x : 0u;
+      b.y = live ? b.y : 0u;
       uint32_t x0, x1, x2, x3;
       dequant8(pick4(j < 4 ? wa0 : wb0, j & 3), x0, x1, x2, x3);
-      if (j & 1) mma_16816(d0, x0, x1, x2, x3, b.x, b.y);
-      else mma_16816(c0, x0, x1, x2, x3, b.x, b.y);
+      mma_16816(c0, x0, x1, x2, x3, b.x, b.y);
       dequant8(pick4(j < 4 ? wa1 : wb1, j & 3), x0, x1, x2, x3);
-      if (j & 1) mma_16816(d1, x0, x1, x2, x3, b.x, b.y);
-      else mma_16816(c1, x0, x1, x2, x3, b.x, b.y);
+      mma_16816(c1, x0, x1, x2, x3, b.x, b.y);
     }
     const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&sc0));
     const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&sc1));
-    acc[0][0] = fmaf(s0.x, c0[0] + d0[0], acc[0][0]);
-    acc[0][1] = fmaf(s0.x, c0[1] + d0[1], acc[0][1]);
-    acc[0][2] = fmaf(s0.y, c0[2] + d0[2], acc[0][2]);
-    acc[0][3] = fmaf(s0.y, c0[3] + d0[3], acc[0][3]);
-    acc[1][0] = fmaf(s1.x, c1[0] + d1[0], acc[1][0]);
-    acc[1][1] = fmaf(s1.x, c1[1] + d1[1], acc[1][1]);
-    acc[1][2] = fmaf(s1.y, c1[2] + d1[2], acc[1][2]);
-    acc[1][3] = fmaf(s1.y, c1[3] + d1[3], acc[1][3]);
+    acc[0][0] = fmaf(s0.x, c0[0], acc[0][0]);
+    acc[0][1] = fmaf(s0.x, c0[1], acc[0][1]);
+    acc[0][2] = fmaf(s0.y, c0[2], acc[0][2]);
+    acc[0][3] = fmaf(s0.y, c0[3], acc[0][3]);
+    acc[1][0] = fmaf(s1.x, c1[0], acc[1][0]);
+    acc[1][1] = fmaf(s1.x, c1[1], acc[1][1]);
+    acc[1][2] = fmaf(s1.y, c1[2], acc[1][2]);
+    acc[1][3] = fmaf(s1.y, c1[3], acc[1][3]);
   }
 }
 

@@ -139,7 +139,8 @@ moe_status moe_register_expert(moe_ctx* ctx, int layer, int expert, const void* 
 size_t moe_expert_blob_bytes(int wfmt, int hidden, int ffn);
 
 /* One MoE layer on T tokens: out[T,H] (fp32) = combine of the routed experts (+ shared)
- * applied to x[T,H] (bf16 bits, row-major).  x and out are device pointers.
+ * applied to x[T,H] (bf16 bits, row-major).  x and out are device pointers, x 8-byte
+ * aligned.
  * Resident mode: fully stream-ordered, never blocks the host, capturable in a CUDA
  * graph.  Streamed mode: blocks the host once per call to read the routing back, then
  * issues the miss copies on a side stream, hits first, each missed expert's kernels
@@ -150,7 +151,8 @@ moe_status moe_forward(moe_ctx* ctx, int layer, const void* x_bf16, float* out, 
 /* One layer of the residual stack, fused:  if y_prev != NULL: x += y_prev;
  * xn = bf16(x / sqrt(mean(x^2) + eps));  y = layer(xn)  (as moe_forward).
  * x fp32 [T,H] in/out, y_prev fp32 [T,H] or NULL (it may be the same buffer as y),
- * xn bf16 bits [T,H] out, y fp32 [T,H] out; all device pointers.  Same bits as
+ * xn bf16 bits [T,H] out, y fp32 [T,H] out; all device pointers, x and y_prev 16-byte
+ * aligned, xn 8-byte aligned (MOE_EINVAL otherwise).  Same bits as
  * moe_residual_rmsnorm followed by moe_forward; for small T the norm runs inside the
  * router kernel instead of a kernel of its own. */
 moe_status moe_forward_residual(moe_ctx* ctx, int layer, float* x, const float* y_prev, uint16_t* xn,
@@ -164,7 +166,7 @@ moe_status moe_get_routing(moe_ctx* ctx, int layer, int* idx, float* w, int* T_o
 /* Residual + RMS norm of the stack that feeds one layer into the next:
  *   if y != NULL: x += y;   xn = bf16(x / sqrt(mean(x^2) + eps))   (no gain),
  * on T rows of H = the context's hidden size; x fp32 [T,H] in/out, y fp32 [T,H],
- * xn bf16 bits [T,H], all device pointers, stream-ordered. */
+ * xn bf16 bits [T,H], all device pointers (x, y 16-byte aligned), stream-ordered. */
 moe_status moe_residual_rmsnorm(moe_ctx* ctx, float* x, const float* y, uint16_t* xn, int T,
                                 float eps, void* stream);
 
@@ -184,15 +186,16 @@ const char* moe_strerror(moe_status s);
  * pool already holds the free device memory, or a host application whose plugin rules
  * forbid allocation.  It runs the router of moe_forward (router GEMV, top-k, softmax
  * renormalised or sigmoid normalised weights) on x bf16 [T,H] with W fp32 [E,H] (device
- * pointers, no context needed) and writes idx int32 [T,k] and w fp32 [T,k] (device) on
+ * pointers, x 8-byte and W 16-byte aligned, no context needed) and writes idx int32
+ * [T,k] and w fp32 [T,k] (device) on
  * `stream`, the same values moe_forward records for moe_get_routing.
  * Scratch: one 1 MiB device array per device, held for the life of the process; calls
- * whose partial logits (E * ceil(H/512) * T floats) and plan do not fit return
+ * whose partial logits ((ceil(H/1024) + 1) * T * E floats) and plan do not fit return
  * MOE_EINVAL.  Limits otherwise as moe_config (T <= 256, E <= 1024, k <= 32, H % 8 == 0).
  * The first call on a device sets that device up (looks up the array's device address
  * and the kernel's shared-memory limit); make it before any stream capture.  Every call
- * shares the array and it keeps the last call's contents (the ticket it needs at zero is
- * cleared by each call on its stream), so calls that overlap on the GPU (different
+ * shares the array and it keeps the last call's contents (the tickets it needs at zero
+ * are cleared by each call on its stream), so calls that overlap on the GPU (different
  * streams, or other threads) race: order them.  Uses the current device. */
 moe_status moe_route_noalloc(const uint16_t* x_bf16, const float* W, int T, int H, int E, int k, int router,
                              int* idx, float* w, void* stream);

@@ -13,10 +13,14 @@ namespace moe {
 
 // Block = 32 output rows x 8 k-slice lanes.  Lane kl sums slices kl, kl+8, ... of each
 // selected expert in slice order; the 8 lane sums are then added in lane order, the
-// experts in rank order, the shared expert last.
-constexpr int CB_ROWS = 32, CB_KL = 8, CB_MAXJ = 33;
+// experts in rank order, the shared expert last.  The (expert, slice) loads of a thread
+// are independent and issued CB_BATCH at a time, so a token's k experts cost one round
+// trip to memory, not k.
+constexpr int CB_ROWS = 32, CB_KL = 8, CB_MAXJ = 33, CB_BATCH = 16;
 __global__ void __launch_bounds__(CB_ROWS * CB_KL) combine_kernel(CombineArgs a) {
   __shared__ float red[CB_KL][CB_MAXJ][CB_ROWS];
+  __shared__ long long s_base[CB_MAXJ];
+  __shared__ float s_w[CB_MAXJ];
   pdl_wait();  // part_d and the plan come from the kernels before
   pdl_launch_dependents();
   const int t = blockIdx.y;
@@ -25,30 +29,49 @@ __global__ void __launch_bounds__(CB_ROWS * CB_KL) combine_kernel(CombineArgs a)
   const int rows32 = cdiv(a.H, 32) * 32;
   const size_t slot_stride = rows32, ks_stride = (size_t)a.pmax * rows32;
   const int nj = a.k + (a.has_shared ? 1 : 0);
-  for (int j = 0; j < nj; ++j) {
+  if (threadIdx.x < nj) {
+    const int j = threadIdx.x;
     int pass, slot;
     if (j < a.k) {
       pass = a.plan.pair_pass[t * a.k + j];
       slot = a.plan.pair_slot[t * a.k + j];
+      s_w[j] = a.plan.w[t * a.k + j];
     } else {
       pass = a.plan.shared_pass[t];
       slot = a.plan.shared_slot[t];
+      s_w[j] = 1.f;
     }
-    float s = 0.f;
-    if (r < a.H) {
-      const float* src = a.part_d + (size_t)pass * a.nks_d * ks_stride + slot * slot_stride + r;
-      for (int k0 = kl; k0 < a.nks_d; k0 += 8 * CB_KL) {  // 8 loads in flight, added in order
-        float v[8];
+    s_base[j] = (long long)pass * a.nks_d * ks_stride + (long long)slot * slot_stride;
+  }
+  for (int j = 0; j < nj; ++j) red[kl][j][rl] = 0.f;
+  __syncthreads();
+  const int nper = kl < a.nks_d ? cdiv(a.nks_d - kl, CB_KL) : 0;   // slices of this lane per expert
+  const int U = r < a.H ? nj * nper : 0;
+  int lj = 0, lm = 0;     // (expert, slice) of the next load
+  int sj = 0, sm = 0;     // (expert, slice) of the next add
+  float run = 0.f;        // running sum of expert sj, in ascending slice order
+  for (int u0 = 0; u0 < U; u0 += CB_BATCH) {
+    float v[CB_BATCH];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int ks = k0 + q * CB_KL;
-          v[q] = ks < a.nks_d ? __ldcg(src + ks * ks_stride) : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) s += v[q];
+    for (int q = 0; q < CB_BATCH; ++q) {
+      v[q] = 0.f;
+      if (u0 + q < U) {
+        v[q] = __ldcg(a.part_d + s_base[lj] + r + (size_t)(kl + CB_KL * lm) * ks_stride);
+        if (++lm == nper) { lm = 0; ++lj; }
       }
     }
-    red[kl][j][rl] = s;
+#pragma unroll
+    for (int q = 0; q < CB_BATCH; ++q) {
+      if (u0 + q < U) {
+        run += v[q];
+        if (++sm == nper) {
+          red[kl][sj][rl] = run;
+          run = 0.f;
+          sm = 0;
+          ++sj;
+        }
+      }
+    }
   }
   __syncthreads();
   if (kl == 0 && r < a.H) {
@@ -57,7 +80,7 @@ __global__ void __launch_bounds__(CB_ROWS * CB_KL) combine_kernel(CombineArgs a)
       float y = 0.f;
 #pragma unroll
       for (int q = 0; q < CB_KL; ++q) y += red[q][j][rl];
-      if (j < a.k) acc = fmaf(a.plan.w[t * a.k + j], y, acc);
+      if (j < a.k) acc = fmaf(s_w[j], y, acc);
       else acc += y;
     }
     const size_t o = (size_t)t * a.H + r;

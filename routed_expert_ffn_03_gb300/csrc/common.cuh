@@ -143,23 +143,33 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }  // namespace moe
 
 namespace moe {
-// 1 / sqrt(mean((x + y)^2) + eps) over one row of H values (y may be null), reduced in a
-// fixed order (thread-strided partial sums, then warp and block trees), so every block
-// that calls it on the same row gets the same bits.  All threads of the block call it;
-// red needs 32 floats.
+// 1 / sqrt(mean((x + y)^2) + eps) over one row of H values (y may be null; H % 4 == 0,
+// rows 16-byte aligned), reduced in a fixed order (thread-strided float4 partial sums,
+// then warp and block trees), so every block that calls it on the same row gets the same
+// bits.  All threads of the block call it; red needs 32 floats.
 __device__ __forceinline__ float block_inv_rms(const float* x, const float* y, int H, float eps, float* red) {
   float ss = 0.f;
-  const int step = blockDim.x;
-  for (int h0 = threadIdx.x; h0 < H; h0 += 8 * step) {  // 8 (x, y) loads in flight, summed in order
-    float v[8];
+  const int step = blockDim.x, n4 = H >> 2;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  const float4* y4 = reinterpret_cast<const float4*>(y);
+  for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * step) {  // 8 (x, y) float4 loads in flight, summed in order
+    float4 v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const int h = h0 + q * step;
-      v[q] = h < H ? __ldcg(x + h) : 0.f;
-      if (y && h < H) v[q] += __ldcg(y + h);
+      const int i = i0 + q * step;
+      v[q] = i < n4 ? __ldcg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (y && i < n4) {
+        const float4 b = __ldcg(y4 + i);
+        v[q].x += b.x; v[q].y += b.y; v[q].z += b.z; v[q].w += b.w;
+      }
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) ss = fmaf(v[q], v[q], ss);
+    for (int q = 0; q < 8; ++q) {
+      ss = fmaf(v[q].x, v[q].x, ss);
+      ss = fmaf(v[q].y, v[q].y, ss);
+      ss = fmaf(v[q].z, v[q].z, ss);
+      ss = fmaf(v[q].w, v[q].w, ss);
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);

@@ -391,7 +391,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   }
   AL(c->d_router, router_bytes);
   AL(c->d_rpart, rpart * sizeof(float));
-  AL(c->d_ticket, sizeof(unsigned int));
+  AL(c->d_ticket, router_tickets(E) * sizeof(unsigned int));
   if (part_gu) AL(c->d_part_gu, part_gu * sizeof(float));
   if (hbuf) AL(c->d_h, hbuf * sizeof(float));
   AL(c->d_part_d, part_d * sizeof(float));
@@ -424,7 +424,7 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     c->plan.small_order = p; p += c->max_pass;
   }
 #undef AL
-  cudaMemset(c->d_ticket, 0, sizeof(unsigned int));
+  cudaMemset(c->d_ticket, 0, router_tickets(E) * sizeof(unsigned int));
   cudaMemset(c->d_status, 0, 4);
   cudaMemset(c->d_counters, 0, sizeof(DevCounters));
   cudaMemset(c->d_plan_mem, 0, 16 * sizeof(int));
@@ -780,6 +780,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
 
 moe_status moe_forward(moe_ctx* c, int layer, const void* x, float* out, int T, void* stream) {
   if (!c || !x || !out || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
+  if ((uintptr_t)x & 7) return MOE_EINVAL;
   if (T < 1 || T > c->cfg.max_tokens) return MOE_EINVAL;
   if (c->sticky != MOE_OK) return c->sticky;
   moe_status rs = layer_ready(c, layer);
@@ -792,6 +793,7 @@ moe_status moe_forward_residual(moe_ctx* c, int layer, float* x, const float* y_
                                 int T, float eps, void* stream) {
   if (!c || !x || !xn || !y || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
   if (T < 1 || T > c->cfg.max_tokens) return MOE_EINVAL;
+  if (((uintptr_t)x & 15) || ((uintptr_t)y_prev & 15) || ((uintptr_t)xn & 7)) return MOE_EINVAL;
   if (c->sticky != MOE_OK) return c->sticky;
   moe_status rs = layer_ready(c, layer);
   if (rs != MOE_OK) return rs;
@@ -822,6 +824,7 @@ moe_status moe_get_routing(moe_ctx* c, int layer, int* idx, float* w, int* T_out
 moe_status moe_residual_rmsnorm(moe_ctx* c, float* x, const float* y, uint16_t* xn, int T, float eps,
                                 void* stream) {
   if (!c || !x || !xn || T < 1) return MOE_EINVAL;
+  if (((uintptr_t)x & 15) || ((uintptr_t)y & 15)) return MOE_EINVAL;
   if (c->sticky != MOE_OK) return c->sticky;
   DeviceGuard dg(c->device);
   CK(launch_residual_rmsnorm(x, y, xn, T, c->cfg.hidden, eps, (cudaStream_t)stream));

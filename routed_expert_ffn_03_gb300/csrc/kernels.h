@@ -19,7 +19,7 @@ struct DevCounters {           // updated on the device by the router's last blo
   unsigned long long forwards, tokens, lookups, bytes_touched, bytes_router;
 };
 
-constexpr int ROUTER_FUSED_MAXT = 256;
+constexpr int ROUTER_FUSED_MAXT = 8;   // tokens of a fused stack step (norm inside the router)
 
 struct RouterArgs {
   const uint16_t* x;     // bf16 [T][H] router input (when xres is null)
@@ -29,8 +29,8 @@ struct RouterArgs {
   float eps;
   const float* W;        // [E][H]
   int T, H, E, k, kind, pmax, has_shared;
-  float* partial;        // [E][nch][T]
-  unsigned int* ticket;  // zero between launches
+  float* partial;        // [router_nch(H)][T][E]: slice partials, then the logits
+  unsigned int* ticket;  // [router_tickets(E)], zero between launches
   PlanPtrs plan;
   int* store_idx;        // per-layer copy of the routing [T][k]
   float* store_w;
@@ -41,6 +41,7 @@ struct RouterArgs {
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s);
 cudaError_t router_set_attributes();
 int router_nch(int H);
+int router_tickets(int E);
 
 // Work over passes: [p_begin, p_end) of the order array (identity when order == null);
 // p_end < 0 means "to the plan's n_pass".

@@ -5,7 +5,7 @@
 // captured), an engine whose own pool already holds all free device memory, or a host
 // application whose plugin rules forbid allocating.  This entry point runs the same
 // router kernel as moe_forward, but its scratch (partial logits, the expert plan, the
-// block ticket) lives in one file-scope device array of fixed size instead of memory the
+// block tickets) lives in one file-scope device array of fixed size instead of memory the
 // context allocates.  The array exists once per device for the life of the process.
 #include <cstring>
 #include <mutex>
@@ -52,12 +52,13 @@ size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 extern "C" moe_status moe_route_noalloc(const uint16_t* x, const float* W, int T, int H, int E, int k, int router,
                                         int* idx, float* w, void* stream) {
   if (!x || !W || !idx || !w) return MOE_EINVAL;
+  if (((uintptr_t)x & 7) || ((uintptr_t)W & 15)) return MOE_EINVAL;
   if (T < 1 || T > 256 || H < 8 || H % 8 || E < 1 || E > 1024 || k < 1 || k > E || k > 32) return MOE_EINVAL;
   if (router != MOE_ROUTER_SOFTMAX_TOPK_RENORM && router != MOE_ROUTER_SIGMOID_TOPK_NORM) return MOE_EINVAL;
-  // scratch layout: ticket | counters | partial logits [E][nch][T] | plan ints
+  // scratch layout: tickets | counters | partial logits [nch][T][E] | plan ints
   const size_t nch = (size_t)moe::router_nch(H);
   const size_t max_pass = (size_t)T * k;  // one token per pass, no shared expert
-  const size_t off_cnt = 256;
+  const size_t off_cnt = align_up((size_t)moe::router_tickets(E) * sizeof(unsigned int));
   const size_t off_part = align_up(off_cnt + sizeof(moe::DevCounters));
   const size_t off_plan = align_up(off_part + (size_t)E * nch * T * sizeof(float));
   const size_t plan_ints = 16 + 3 * max_pass + 4 * (size_t)T * k + 2 * (size_t)T + E;
@@ -72,7 +73,7 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, const float* W, int T
   moe_status st = setup_device(dev, &base);
   if (st != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  // the array keeps the previous call's contents: the ticket must start at zero
+  // the array keeps the previous call's contents: the tickets must start at zero
   if (cudaMemsetAsync(base, 0, off_part, s) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ECUDA;

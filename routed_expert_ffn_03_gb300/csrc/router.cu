@@ -12,13 +12,16 @@
 // uses xn = bf16((x + y_prev) * inv) as the router input and writes its slice of xn for
 // the expert kernels; the residual x += y_prev is written later by the combine kernel,
 // which reads y_prev just before it overwrites y.
-// Phase 1 (all blocks): each warp owns (expert e, 512-wide chunk c of H) and writes the
-// partial dot products of all T tokens.  Phase 2 (the block that arrives last, found
-// with an atomic ticket; no block waits on another): sums the partials in chunk order
-// (all (token, expert) pairs in parallel),
-// selects the top-k per token (one warp per token), and buckets the (token, rank) pairs
-// by expert into "passes" of up to pmax tokens: routed experts in ascending id, tokens
-// ascending, then the shared expert.
+// Phase 1 (all blocks): block (s, g) owns the 1024-wide slice s of H and the group g of
+// 8 experts, one per warp.  A warp loads its expert's slice of W into registers before
+// it waits on the kernel before (the weights do not depend on it), the block stages the
+// slice of the bf16 router input in shared memory, and the warp writes the partial dot
+// products of all T tokens.  The last block of a group to finish (an atomic ticket per
+// group) adds the group's partials in slice order into the logits; the last group to
+// finish (a second ticket) runs phase 2: the top-k per token (one warp per token,
+// straight from the logits) and the bucketing of the (token, rank) pairs by expert into
+// "passes" of up to pmax tokens: routed experts in ascending id, tokens ascending, then
+// the shared expert.  No block ever waits on another.
 #include <cfloat>
 
 #include "common.cuh"
@@ -26,8 +29,17 @@
 
 namespace moe {
 
-constexpr int RCH = 512;
-int router_nch(int H) { return cdiv(H, RCH); }
+constexpr int RSW = 1024;   // inputs per slice: 8 float4 of W per lane
+constexpr int REPB = 8;     // experts per block (one per warp)
+constexpr int RTG = 32;     // tokens staged per pass over the slice
+constexpr int RXS_BYTES = RTG * RSW * 2;
+constexpr int RNS_ONE = 8;                 // the last block adds the slices itself when
+constexpr size_t RSUM_ONE_BLOCK = 16384;   // NS <= RNS_ONE and NS * T * E <= RSUM_ONE_BLOCK
+__host__ __device__ __forceinline__ bool router_two_level(int NS, int T, int E) {
+  return NS > RNS_ONE || (size_t)NS * T * E > RSUM_ONE_BLOCK;
+}
+int router_nch(int H) { return cdiv(H, RSW) + 1; }     // slices of partials + the logits
+int router_tickets(int E) { return cdiv(E, REPB) + 1; }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -35,186 +47,246 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-constexpr int LOGIT_SMEM = 8192;  // floats of logits staged per chunk of tokens
+// dense-group split of an expert's c tokens (pmax == 1): chunks of <= GEMM_MAX_TOKENS
+__device__ __forceinline__ int big_chunks(int c, int big_min) {
+  return (big_min > 0 && c >= big_min) ? cdiv(c, GEMM_MAX_TOKENS) : 0;
+}
 
 __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
-  extern __shared__ int sm[];
+  extern __shared__ __align__(16) int sm[];
   __shared__ float s_inv[ROUTER_FUSED_MAXT];
   __shared__ float s_red[32];
+  __shared__ int s_flag, s_routed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  const int nch = cdiv(a.H, RCH);
-  const int nitems = a.E * nch;
+  const int NS = cdiv(a.H, RSW), NG = cdiv(a.E, REPB);
+  const int sl = blockIdx.x % NS, g = blockIdx.x / NS;
+  const int h0 = sl * RSW;
+  const int e = g * REPB + warp;
+  const bool live = e < a.E;
   const bool fused = a.xres != nullptr;
+
+  // ---------------- W slice of this warp's expert (independent of the kernel before)
+  float4 wv[RSW / 128];
+  {
+    const float* wr = a.W + (size_t)(live ? e : 0) * a.H;
+#pragma unroll
+    for (int i = 0; i < RSW / 128; ++i) {
+      const int h = h0 + 4 * (lane + 32 * i);
+      wv[i] = (live && h < a.H) ? __ldg(reinterpret_cast<const float4*>(wr + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
 
   pdl_wait();  // x (and the residual) come from the kernels before
   pdl_launch_dependents();
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);   // [RTG][RSW] bf16 router input
   if (fused) {
+    // fused stack step (T <= ROUTER_FUSED_MAXT): this thread's float4 of the slice for
+    // every token is loaded together with the norm's loads, then normalised and staged;
+    // the blocks of group 0 also write their slice of xn for the expert kernels
+    const int hq = 4 * threadIdx.x, h = h0 + hq;
+    const bool in = threadIdx.x < RSW / 4 && h < a.H;
+    float4 xv[ROUTER_FUSED_MAXT];
+#pragma unroll
+    for (int t = 0; t < ROUTER_FUSED_MAXT; ++t) {
+      xv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < a.T && in) {
+        const size_t o = (size_t)t * a.H + h;
+        xv[t] = __ldcg(reinterpret_cast<const float4*>(a.xres + o));
+        if (a.yprev) {
+          const float4 y4 = __ldcg(reinterpret_cast<const float4*>(a.yprev + o));
+          xv[t].x += y4.x; xv[t].y += y4.y; xv[t].z += y4.z; xv[t].w += y4.w;
+        }
+      }
+    }
     for (int t = 0; t < a.T; ++t) {
       const float inv = block_inv_rms(a.xres + (size_t)t * a.H, a.yprev ? a.yprev + (size_t)t * a.H : nullptr,
                                       a.H, a.eps, s_red);
       if (threadIdx.x == 0) s_inv[t] = inv;
     }
     __syncthreads();
-  }
-
-  if (fused) {
-    // xn is not read by this kernel: each block writes a disjoint slice of it
-    const int per = cdiv(a.H, gridDim.x);
-    for (int t = 0; t < a.T; ++t) {
-      const float inv = s_inv[t];
-      for (int h = blockIdx.x * per + threadIdx.x; h < min(a.H, (blockIdx.x + 1) * per); h += blockDim.x) {
-        const size_t o = (size_t)t * a.H + h;
-        float v = __ldcg(a.xres + o);
-        if (a.yprev) v += __ldcg(a.yprev + o);
-        a.xn_out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(v * inv));
+#pragma unroll
+    for (int t = 0; t < ROUTER_FUSED_MAXT; ++t) {
+      if (t < a.T && threadIdx.x < RSW / 4) {
+        const float inv = s_inv[t];
+        uint2 v;
+        v.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].x * inv)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].y * inv)) << 16);
+        v.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].z * inv)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].w * inv)) << 16);
+        if (!in) v = make_uint2(0u, 0u);
+        *reinterpret_cast<uint2*>(xs + t * RSW + hq) = v;
+        if (g == 0 && in) *reinterpret_cast<uint2*>(a.xn_out + (size_t)t * a.H + h) = v;
       }
     }
   }
 
-  // ---------------- phase 1: partial logits
-  for (int item = blockIdx.x * nwarps + warp; item < nitems; item += gridDim.x * nwarps) {
-    const int e = item / nch, c = item % nch;
-    const int h0 = c * RCH, h1 = min(a.H, h0 + RCH);
-    const float* wr = a.W + (size_t)e * a.H;
-    for (int t0 = 0; t0 < a.T; t0 += 8) {
-      const int nt = min(8, a.T - t0);
-      float acc[8];
+  // ---------------- phase 1: partial logits of slice sl, partial[sl][t][e]
+  for (int tg = 0; tg < a.T; tg += RTG) {
+    const int nt = min(RTG, a.T - tg);
+    __syncthreads();  // the previous group's reads of xs are done (fused: xs is staged)
+    if (!fused) {
+      for (int q = threadIdx.x; q < nt * (RSW / 4); q += blockDim.x) {
+        const int tl = q / (RSW / 4), hq = 4 * (q % (RSW / 4)), h = h0 + hq;
+        uint2 v = make_uint2(0u, 0u);
+        if (h < a.H) v = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)(tg + tl) * a.H + h));
+        *reinterpret_cast<uint2*>(xs + tl * RSW + hq) = v;
+      }
+      __syncthreads();
+    }
+    if (live) {
+      float keep = 0.f;
+      for (int tl = 0; tl < nt; ++tl) {
+        const uint16_t* xr = xs + tl * RSW;
+        float acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int h = h0 + lane * 4; h < h1; h += 128) {
-        const float4 wv = __ldg(reinterpret_cast<const float4*>(wr + h));
-#pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          if (tt < nt) {
-            float x0, x1, x2, x3;
-            if (fused) {
-              const size_t o = (size_t)(t0 + tt) * a.H + h;
-              float4 v = __ldcg(reinterpret_cast<const float4*>(a.xres + o));
-              if (a.yprev) {
-                const float4 y = __ldcg(reinterpret_cast<const float4*>(a.yprev + o));
-                v.x += y.x; v.y += y.y; v.z += y.z; v.w += y.w;
-              }
-              const float inv = s_inv[t0 + tt];
-              x0 = __bfloat162float(__float2bfloat16_rn(v.x * inv));
-              x1 = __bfloat162float(__float2bfloat16_rn(v.y * inv));
-              x2 = __bfloat162float(__float2bfloat16_rn(v.z * inv));
-              x3 = __bfloat162float(__float2bfloat16_rn(v.w * inv));
-            } else {
-              const uint2 xb = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)(t0 + tt) * a.H + h));
-              x0 = __uint_as_float(xb.x << 16);
-              x1 = __uint_as_float(xb.x & 0xffff0000u);
-              x2 = __uint_as_float(xb.y << 16);
-              x3 = __uint_as_float(xb.y & 0xffff0000u);
-            }
-            acc[tt] = fmaf(wv.x, x0, acc[tt]);
-            acc[tt] = fmaf(wv.y, x1, acc[tt]);
-            acc[tt] = fmaf(wv.z, x2, acc[tt]);
-            acc[tt] = fmaf(wv.w, x3, acc[tt]);
-          }
+        for (int i = 0; i < RSW / 128; ++i) {
+          const uint2 xb = *reinterpret_cast<const uint2*>(xr + 4 * (lane + 32 * i));
+          acc = fmaf(wv[i].x, __uint_as_float(xb.x << 16), acc);
+          acc = fmaf(wv[i].y, __uint_as_float(xb.x & 0xffff0000u), acc);
+          acc = fmaf(wv[i].z, __uint_as_float(xb.y << 16), acc);
+          acc = fmaf(wv[i].w, __uint_as_float(xb.y & 0xffff0000u), acc);
         }
+        acc = warp_sum(acc);
+        if (lane == tl) keep = acc;
       }
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        const float v = warp_sum(acc[tt]);
-        if (lane == 0 && tt < nt) a.partial[((size_t)e * nch + c) * a.T + t0 + tt] = v;
-      }
+      if (lane < nt) a.partial[((size_t)sl * a.T + tg + lane) * a.E + e] = keep;
     }
   }
 
-  // ---------------- ticket: the last block continues
-  __shared__ int s_last, s_routed;
+  // ---------------- tickets.  Small problems: the last block overall adds the slices
+  // itself.  Otherwise the last block of each expert group adds its group's slices into
+  // the logits, and the last group continues.  Both add the slices in ascending order.
+  const bool two_level = router_two_level(NS, a.T, a.E);
+  float* logits = a.partial + (size_t)NS * a.T * a.E;   // [T][E] (two-level only)
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned int tk = atomicAdd(a.ticket, 1u);
-    s_last = (tk == gridDim.x - 1);
+  if (two_level) {
+    if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket + 1 + g, 1u) == (unsigned)NS - 1);
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    const int ne = min(REPB, a.E - g * REPB);
+    for (int q = threadIdx.x; q < a.T * ne; q += blockDim.x) {
+      const int t = q / ne, ee = g * REPB + q % ne;
+      const float* pp = a.partial + (size_t)t * a.E + ee;
+      float v = 0.f;
+#pragma unroll 8
+      for (int ss = 0; ss < NS; ++ss) v += __ldcg(pp + (size_t)ss * a.T * a.E);
+      logits[(size_t)t * a.E + ee] = v;
+    }
+    if (threadIdx.x == 0) a.ticket[1 + g] = 0u;  // ready for the next launch (stream-ordered)
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket, 1u) == (unsigned)NG - 1);
+  } else {
+    if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket, 1u) == gridDim.x - 1);
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!s_flag) return;
   __threadfence();
 
   const int E = a.E, T = a.T, k = a.k, pmax = a.pmax;
-  float* slog = reinterpret_cast<float*>(sm);   // [tc][E]
-  int* s_cnt = sm + LOGIT_SMEM;                 // [E]
-  int* s_off = s_cnt + E;                       // [E]
-  int* s_idx = s_off + E;                       // [T*k]
-  int* s_pos = s_idx + T * k;                   // [T*k]
-
-
-  // ---------------- phase 2a: logits (all (t, e) in parallel), then top-k per token
-  const int tc = max(1, min(T, LOGIT_SMEM / E));
-  for (int tb = 0; tb < T; tb += tc) {
-    const int nt = min(tc, T - tb);
-    for (int q = threadIdx.x; q < nt * E; q += blockDim.x) {
-      const int tl = q / E, e = q % E;
-      const float* pp = a.partial + (size_t)e * nch * T + tb + tl;
-      float s = 0.f;
-#pragma unroll 8
-      for (int c = 0; c < nch; ++c) s += __ldcg(pp + (size_t)c * T);
-      slog[tl * E + e] = s;
+  int* s_cnt = sm;                  // [E]
+  int* s_off = s_cnt + E;           // [E]
+  int* s_idx = s_off + E;           // [T*k]
+  int* s_pos = s_idx + T * k;       // [T*k]
+  float* slog = reinterpret_cast<float*>(s_pos + T * k);   // [T][E] (single-level only)
+  for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
+  if (!two_level) {
+    // logits = slice partials added in ascending slice order, all (t, e) in parallel
+    const size_t TE = (size_t)T * E;
+    for (int q0 = threadIdx.x; q0 < (int)TE; q0 += 2 * blockDim.x) {
+      float p[2][RNS_ONE];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = q0 + u * blockDim.x;
+#pragma unroll
+        for (int ss = 0; ss < RNS_ONE; ++ss) p[u][ss] = (ss < NS && q < (int)TE) ? __ldcg(a.partial + ss * TE + q) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = q0 + u * blockDim.x;
+        float v = 0.f;
+#pragma unroll
+        for (int ss = 0; ss < RNS_ONE; ++ss)
+          if (ss < NS) v += p[u][ss];
+        if (q < (int)TE) slog[q] = v;
+      }
     }
-    __syncthreads();
-    for (int tl = warp; tl < nt; tl += nwarps) {
-      const int t = tb + tl;
-      float v[32];
+  }
+  __syncthreads();
+
+  // ---------------- phase 2a: top-k per token (one warp per token)
+  for (int t = warp; t < T; t += nwarps) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int ee = lane + 32 * i;
+      v[i] = ee < E ? (two_level ? __ldcg(logits + (size_t)t * E + ee) : slog[t * E + ee]) : -INFINITY;
+    }
+    // each lane keeps the maximum of its own experts not yet taken; the warp takes the
+    // best k times, and only the lane that gave its maximum away looks for its next one.
+    // NaN ranks as -inf; equal values rank the lower id first.
+    uint32_t taken = 0u;
+    auto lane_best = [&](float& bv, int& be) {
+      bv = -INFINITY;
+      be = 0x7fffffff;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? slog[tl * E + e] : -INFINITY;
+        const int ee = lane + 32 * i;
+        const float x = v[i] != v[i] ? -INFINITY : v[i];
+        if (ee < E && !((taken >> i) & 1u) && (x > bv || (x == bv && ee < be))) { bv = x; be = ee; }
       }
-      int my_e = 0;
-      float my_l = 0.f;
-      for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
+    };
+    float lv;
+    int le;
+    lane_best(lv, le);
+    int my_e = 0;
+    float my_l = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bv = lv;
+      int be = le;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (lane + 32 * i == be) v[i] = -INFINITY;
-        if (lane == j) { my_e = be; my_l = bv; }
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
       }
-      // weights over the k selected (rank order = lane order)
-      const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-      float num = 0.f;
-      if (lane < k) {
-        if (a.kind == 0) num = expf(my_l - lmax);
-        else num = 1.f / (1.f + expf(-my_l));
-      }
-      float den = num;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-      if (lane < k) {
-        const float w = num / den;
-        a.plan.idx[t * k + lane] = my_e;
-        a.plan.w[t * k + lane] = w;
-        a.store_idx[t * k + lane] = my_e;
-        a.store_w[t * k + lane] = w;
-        s_idx[t * k + lane] = my_e;
+      if (lane == j) { my_e = be; my_l = bv; }
+      if (be == le) {   // this lane's maximum was taken (ids are distinct across lanes)
+        taken |= 1u << ((be - lane) >> 5);
+        lane_best(lv, le);
       }
     }
-    __syncthreads();
+    // weights over the k selected (rank order = lane order)
+    const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+    float num = 0.f;
+    if (lane < k) {
+      if (a.kind == 0) num = expf(my_l - lmax);
+      else num = 1.f / (1.f + expf(-my_l));
+    }
+    float den = num;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane < k) {
+      const float w = num / den;
+      a.plan.idx[t * k + lane] = my_e;
+      a.plan.w[t * k + lane] = w;
+      a.store_idx[t * k + lane] = my_e;
+      a.store_w[t * k + lane] = w;
+      s_idx[t * k + lane] = my_e;
+    }
   }
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
 
   // ---------------- phase 2b: position of each pair within its expert (tokens ascending)
   if (warp == 0) {
     for (int t = 0; t < T; ++t) {
       if (lane < k) {
-        const int e = s_idx[t * k + lane];   // the k experts of a token are distinct
-        const int pos = s_cnt[e];
-        s_cnt[e] = pos + 1;
+        const int ee = s_idx[t * k + lane];   // the k experts of a token are distinct
+        const int pos = s_cnt[ee];
+        s_cnt[ee] = pos + 1;
         s_pos[t * k + lane] = pos;
       }
       __syncwarp();
@@ -223,9 +295,9 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
     const int run = cdiv(E, 32);
     const int e0 = min(E, lane * run), e1 = min(E, e0 + run);
     int np = 0, nu = 0;
-    for (int e = e0; e < e1; ++e) {
-      np += cdiv(s_cnt[e], pmax);
-      nu += s_cnt[e] > 0;
+    for (int ee = e0; ee < e1; ++ee) {
+      np += cdiv(s_cnt[ee], pmax);
+      nu += s_cnt[ee] > 0;
     }
     int inp = np, inu = nu;
 #pragma unroll
@@ -235,10 +307,10 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
       if (lane >= o) { inp += a1; inu += a2; }
     }
     int off = inp - np, uoff = inu - nu;
-    for (int e = e0; e < e1; ++e) {
-      s_off[e] = off;
-      const int c = s_cnt[e];
-      if (c > 0) a.plan.uniq[uoff++] = e;
+    for (int ee = e0; ee < e1; ++ee) {
+      s_off[ee] = off;
+      const int c = s_cnt[ee];
+      if (c > 0) a.plan.uniq[uoff++] = ee;
       off += cdiv(c, pmax);
     }
     const int tot_p = __shfl_sync(0xffffffffu, inp, 31);
@@ -262,16 +334,16 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 
   // ---------------- phase 2c: pass tables
   const int routed_passes = s_routed;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int c = s_cnt[e];
+  for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
+    const int c = s_cnt[ee];
     for (int i = 0; i * pmax < c; ++i) {
-      a.plan.pass_expert[s_off[e] + i] = e;
-      a.plan.pass_ntok[s_off[e] + i] = min(pmax, c - i * pmax);
+      a.plan.pass_expert[s_off[ee] + i] = ee;
+      a.plan.pass_ntok[s_off[ee] + i] = min(pmax, c - i * pmax);
     }
   }
   for (int q = threadIdx.x; q < T * k; q += blockDim.x) {
-    const int e = s_idx[q], pos = s_pos[q];
-    const int pass = s_off[e] + pos / pmax, slot = pos % pmax;
+    const int ee = s_idx[q], pos = s_pos[q];
+    const int pass = s_off[ee] + pos / pmax, slot = pos % pmax;
     a.plan.pass_tok[pass * pmax + slot] = q / k;
     a.plan.pair_pass[q] = pass;
     a.plan.pair_slot[q] = slot;
@@ -290,34 +362,55 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
   }
   // dense groups (pmax == 1: one pass per token): experts with >= big_min tokens go to the
   // tcgen05 path in balanced chunks of <= GEMM_MAX_TOKENS, every other pass to the
-  // per-token path, both lists in ascending expert id then token order
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int nb = 0, ns = 0;
-    auto emit = [&](int expert, int first, int c) {
-      if (a.big_min > 0 && c >= a.big_min) {
-        const int nch = cdiv(c, GEMM_MAX_TOKENS), base = c / nch, rem = c % nch;
-        int start = 0;
-        for (int q = 0; q < nch; ++q) {
-          const int sz = base + (q < rem ? 1 : 0);
-          a.plan.big[3 * nb + 0] = expert;
-          a.plan.big[3 * nb + 1] = first + start;
-          a.plan.big[3 * nb + 2] = sz;
-          ++nb;
-          start += sz;
-        }
-      } else if (a.big_min > 0) {
-        for (int i = 0; i < c; ++i) a.plan.small_order[ns++] = first + i;
-      }
-    };
+  // per-token path, both lists in ascending expert id (the shared expert last) then token
+  // order.  Warp 0: lane owns a contiguous run of experts, an exclusive scan places it.
+  if (warp == 0) {
     if (a.big_min > 0) {
-      for (int e = 0; e < E; ++e)
-        if (s_cnt[e] > 0) emit(e, s_off[e], s_cnt[e]);
-      if (a.has_shared) emit(E, routed_passes, T);
+      const int E1 = E + (a.has_shared ? 1 : 0);
+      const int run = cdiv(E1, 32);
+      const int e0 = min(E1, lane * run), e1 = min(E1, e0 + run);
+      auto cnt_of = [&](int ee) { return ee < E ? s_cnt[ee] : T; };
+      auto first_of = [&](int ee) { return ee < E ? s_off[ee] : routed_passes; };
+      int nb = 0, ns = 0;
+      for (int ee = e0; ee < e1; ++ee) {
+        const int c = cnt_of(ee), nc = big_chunks(c, a.big_min);
+        nb += nc;
+        ns += nc ? 0 : c;
+      }
+      int ib = nb, is = ns;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a1 = __shfl_up_sync(0xffffffffu, ib, o);
+        const int a2 = __shfl_up_sync(0xffffffffu, is, o);
+        if (lane >= o) { ib += a1; is += a2; }
+      }
+      int ob = ib - nb, os = is - ns;
+      for (int ee = e0; ee < e1; ++ee) {
+        const int c = cnt_of(ee), first = first_of(ee), nc = big_chunks(c, a.big_min);
+        if (nc) {
+          const int base = c / nc, rem = c % nc;
+          int start = 0;
+          for (int q = 0; q < nc; ++q) {
+            const int sz = base + (q < rem ? 1 : 0);
+            a.plan.big[3 * ob + 0] = ee;
+            a.plan.big[3 * ob + 1] = first + start;
+            a.plan.big[3 * ob + 2] = sz;
+            ++ob;
+            start += sz;
+          }
+        } else {
+          for (int i = 0; i < c; ++i) a.plan.small_order[os++] = first + i;
+        }
+      }
+      if (lane == 31) {
+        a.plan.hdr->n_big = ib;
+        a.plan.hdr->n_small = is;
+      }
+    } else if (lane == 0) {
+      a.plan.hdr->n_big = 0;
+      a.plan.hdr->n_small = routed_passes + (a.has_shared ? cdiv(T, pmax) : 0);
     }
-    a.plan.hdr->n_big = nb;
-    a.plan.hdr->n_small = a.big_min > 0 ? ns : routed_passes + (a.has_shared ? cdiv(T, pmax) : 0);
-    *a.ticket = 0u;  // ready for the next launch (stream-ordered)
+    if (lane == 0) *a.ticket = 0u;  // ready for the next launch (stream-ordered)
   }
 }
 
@@ -326,13 +419,16 @@ cudaError_t router_set_attributes() {
                               160 * 1024);
 }
 
+size_t router_smem_bytes(int H, int T, int E, int k) {
+  const size_t p2 = (size_t)(2 * E + 2 * T * k) * sizeof(int) +
+                    (router_two_level(cdiv(H, RSW), T, E) ? 0 : (size_t)T * E * sizeof(float));
+  return std::max((size_t)RXS_BYTES, p2);
+}
+
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s) {
-  const int nch = router_nch(a.H);
-  const int nitems = a.E * nch;
-  int grid = cdiv(nitems, 8);
-  grid = std::max(1, std::min(grid, num_sms));
-  const size_t smem = (size_t)(LOGIT_SMEM + 2 * a.E + 2 * a.T * a.k) * sizeof(int);
-  return launch_pdl(router_kernel, grid, 256, smem, s, a);
+  (void)num_sms;
+  const int grid = cdiv(a.H, RSW) * cdiv(a.E, REPB);
+  return launch_pdl(router_kernel, grid, 256, router_smem_bytes(a.H, a.T, a.E, a.k), s, a);
 }
 
 }  // namespace moe

@@ -27,7 +27,10 @@
 // row block, matrix, k-slice) order; down tasks in (pass, k-slice, row block) order and
 // leave k-slice partials for the combine kernel.  The B fragments are kept only for the
 // mma columns that carry tokens (2 per token), which leaves room for 3 ring slots per
-// warp when a pass has one token.
+// warp when a pass has one token.  They are stored per column, k-steps contiguous (two
+// k-steps per 16-byte load, columns padded so the lanes of a load hit distinct banks);
+// a lane whose column carries no token reads a live column instead, and its results
+// land in mma columns nobody reads.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -38,15 +41,20 @@ constexpr int I4_SLICE_KSTEPS = I4_KS * I4_GROUP / 16;   // 16 mma k-steps per s
 constexpr int I4_MAX_RECS = 512;                         // passes one block may touch
 constexpr int I4_STATIC_SMEM = I4_MAX_RECS * 8 + 128;
 
+// B fragments: [column][k-step] uint2, column stride kstride(n k-steps) = n + 2 (16 B of
+// padding: consecutive columns start 4 or 20 banks apart, so the 8 columns of a 16-byte
+// load phase are conflict-free).
+__host__ __device__ constexpr int i4_kstride(int nks16) { return nks16 + 2; }
+
 // nb = mma columns that carry data (2 per token of the widest pass).
 template <int NW, int D>
 struct I4Smem {
   static constexpr int ring = NW * D * I4_STAGE;
   static constexpr int bars = NW * D * 8;
-  static constexpr int gateup(int H, int nb) { return ring + bars + (H / 16) * nb * 4 * 8; }
+  static constexpr int gateup(int H, int nb) { return ring + bars + nb * 4 * i4_kstride(H / 16) * 8; }
   // down keeps B fragments for all 8 columns (one slice is small) and the slice inputs
   static constexpr int down() {
-    return ring + bars + I4_SLICE_KSTEPS * 8 * 4 * 8 + I4_PMAX * I4_KS * I4_GROUP * 4;
+    return ring + bars + 8 * 4 * i4_kstride(I4_SLICE_KSTEPS) * 8 + I4_PMAX * I4_KS * I4_GROUP * 4;
   }
 };
 
@@ -84,34 +92,34 @@ __device__ __forceinline__ uint32_t pick4(const uint4& v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
-// One task: 32 rows x ng (<= 2) groups from a stage; adds W . x into acc[tile][4].
-// xf: B fragments of the task's first k-step, [k-step][g < nb][p] uint2 (lanes with
-// g >= nb hold zero columns and load nothing).
-__device__ __forceinline__ void i4_task(const uint8_t* st, int ng, const uint2* xf, int lane, int nb,
-                                        float (&acc)[2][4]) {
-  const int gq = lane >> 2;
-  for (int gi = 0; gi < ng; ++gi) {
-    const uint8_t* blk = st + gi * I4_PAIR_BLOCK;
-    const uint4 wa0 = *reinterpret_cast<const uint4*>(blk + lane * 16);
-    const uint4 wb0 = *reinterpret_cast<const uint4*>(blk + 512 + lane * 16);
-    const uint4 wa1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK + lane * 16);
-    const uint4 wb1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK + 512 + lane * 16);
-    const uint32_t sc0 = *reinterpret_cast<const uint32_t*>(blk + 1024 + gq * 4);
-    const uint32_t sc1 = *reinterpret_cast<const uint32_t*>(blk + I4_BLOCK + 1024 + gq * 4);
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    // lanes whose mma column carries no token read a zero fragment (no branch)
-    const uint2* xg = xf + gi * 8 * nb * 4 + (gq < nb ? lane : 0);
-    const bool live = gq < nb;
+// One task: 32 rows x NGRP (<= 2) groups from a stage; adds W . x into acc[tile][4].
+// stl = stage + 16 * lane, sts = stage + 1024 + 4 * (lane / 4) (the lane's scale word),
+// xl = the lane's B-fragment column at the task's first k-step.
+template <int NGRP>
+__device__ __forceinline__ void i4_task(const uint8_t* stl, const uint8_t* sts, const uint2* xl, float (&acc)[2][4]) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint2 b = xg[j * nb * 4];
-      b.x = live ? b.x : 0u;
-      b.y = live ? b.y : 0u;
-      uint32_t x0, x1, x2, x3;
-      dequant8(pick4(j < 4 ? wa0 : wb0, j & 3), x0, x1, x2, x3);
-      mma_16816(c0, x0, x1, x2, x3, b.x, b.y);
-      dequant8(pick4(j < 4 ? wa1 : wb1, j & 3), x0, x1, x2, x3);
-      mma_16816(c1, x0, x1, x2, x3, b.x, b.y);
+  for (int gi = 0; gi < NGRP; ++gi) {
+    const uint8_t* blk = stl + gi * I4_PAIR_BLOCK;
+    const uint4 wa0 = *reinterpret_cast<const uint4*>(blk);
+    const uint4 wb0 = *reinterpret_cast<const uint4*>(blk + 512);
+    const uint4 wa1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK);
+    const uint4 wb1 = *reinterpret_cast<const uint4*>(blk + I4_BLOCK + 512);
+    const uint32_t sc0 = *reinterpret_cast<const uint32_t*>(sts + gi * I4_PAIR_BLOCK);
+    const uint32_t sc1 = *reinterpret_cast<const uint32_t*>(sts + gi * I4_PAIR_BLOCK + I4_BLOCK);
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint4 bb = *reinterpret_cast<const uint4*>(xl + gi * 8 + 2 * jj);   // k-steps 2jj, 2jj+1
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = 2 * jj + h;
+        const uint32_t b0 = h ? bb.z : bb.x, b1 = h ? bb.w : bb.y;
+        uint32_t x0, x1, x2, x3;
+        dequant8(pick4(j < 4 ? wa0 : wb0, j & 3), x0, x1, x2, x3);
+        mma_16816(c0, x0, x1, x2, x3, b0, b1);
+        dequant8(pick4(j < 4 ? wa1 : wb1, j & 3), x0, x1, x2, x3);
+        mma_16816(c1, x0, x1, x2, x3, b0, b1);
+      }
     }
     const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&sc0));
     const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&sc1));
@@ -124,6 +132,13 @@ __device__ __forceinline__ void i4_task(const uint8_t* st, int ng, const uint2* 
     acc[1][2] = fmaf(s1.y, c1[2], acc[1][2]);
     acc[1][3] = fmaf(s1.y, c1[3], acc[1][3]);
   }
+}
+
+// The B-fragment column a lane reads: its own (token slot g/2, part g%2, pair p) when
+// g < nb, else the same pair of a live column.
+__device__ __forceinline__ int i4_lane_col(int lane, int nb) {
+  const int gq = lane >> 2;
+  return (gq < nb ? gq : gq % nb) * 4 + (lane & 3);
 }
 
 // B fragment of mma column n = g (token slot n/2, part n%2) for one k-step: elements
@@ -141,19 +156,19 @@ __device__ __forceinline__ uint2 bfrag(const float* v, int part) {
 }
 
 // B fragments of one pass's tokens for nks16 k-steps from fp32 values val(ts, k)
-// (k relative to the first k-step), into xf[k-step][g < nb][p].
+// (k relative to the first k-step), into xf[column n*4 + p][k-step] (stride kstride).
 template <class Val>
 __device__ __forceinline__ void build_bfrags(uint2* xf, int nks16, int nb, int tid, int nthr, Val val) {
-  const int per = nb * 4;
+  const int per = nb * 4, ks = i4_kstride(nks16);
   for (int e = tid; e < nks16 * per; e += nthr) {
-    const int kk = e / per, r = e - kk * per, n = r >> 2, pp = r & 3;
+    const int kk = e / per, col = e - kk * per, n = col >> 2, pp = col & 3;
     float f[10];
     const int kb = kk * 16 + 2 * pp;
     f[0] = val(n >> 1, kb);
     f[1] = val(n >> 1, kb + 1);
     f[8] = val(n >> 1, kb + 8);
     f[9] = val(n >> 1, kb + 9);
-    xf[e] = bfrag(f, n & 1);
+    xf[col * ks + kk] = bfrag(f, n & 1);
   }
 }
 
@@ -175,9 +190,9 @@ __device__ __forceinline__ int pass_of(const ExpertArgs& a, int p_begin, int pi)
 }
 
 // Wait for a full slot (all lanes agree); on a time-out the block is marked aborted.
-template <int D>
-__device__ __forceinline__ bool stage_wait(uint32_t bar, int j, volatile int* abort, const ExpertArgs& a, int lane) {
-  bool ok = !*abort && mbar_wait_bounded(bar, (j / D) & 1, a.budget);
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, volatile int* abort, const ExpertArgs& a,
+                                           int lane) {
+  bool ok = !*abort && mbar_wait_bounded(bar, parity, a.budget);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && !*abort && lane == 0) {
     *abort = 1;
@@ -244,15 +259,15 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
   const int nw = first < t1 ? (t1 - first + NW - 1) / NW : 0;
   int ipi = first / per_pass, irb = (first - ipi * per_pass) / per_rb;   // issue cursor
   int it = first - ipi * per_pass - irb * per_rb;
-  int j_issue = 0;
+  int j_issue = 0, islot = 0;
   auto issue_next = [&]() {
     const int m = it >= nks ? 1 : 0, ks = it - m * nks;
     const int ng = min(I4_KS, NG - ks * I4_KS);
     const uint8_t* src = s_rec[ipi - pi0] + (m ? rg.off[1] : rg.off[0]) +
                          ((size_t)irb * NG + (size_t)ks * I4_KS) * I4_PAIR_BLOCK;
-    const int slot = j_issue % D;
-    stage_issue(lane, full0 + 8 * slot, ring0 + slot * I4_STAGE, src, (uint32_t)ng * I4_PAIR_BLOCK);
+    stage_issue(lane, full0 + 8 * islot, ring0 + islot * I4_STAGE, src, (uint32_t)ng * I4_PAIR_BLOCK);
     ++j_issue;
+    if (++islot == D) islot = 0;
     it += NW;
     while (it >= per_rb) {
       it -= per_rb;
@@ -264,6 +279,8 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
   const int gq = lane >> 2, p = lane & 3;
   const uint8_t* myring = smem + warp * D * I4_STAGE;
   int j = 0;                                 // tasks consumed by this warp
+  int cslot = 0;                             // its ring slot and that slot's phase parity
+  uint32_t cphase = 0u;
   int ti = first;
   for (int seg = t0; seg < t1;) {            // segments = one pass each
     const int pi = seg / per_pass;
@@ -284,19 +301,25 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
     });
     named_sync(1, nthr);
     float* part = a.part_gu + (size_t)pass * 2 * nks * I4_PMAX * rows32;
+    const uint2* xcol = xfrag + i4_lane_col(lane, nb) * i4_kstride(a.H / 16);
     int local = ti - pi * per_pass;          // compute cursor within the pass
     int rb = local / per_rb, t = local - rb * per_rb;
     for (; ti < seg_end; ti += NW) {
       const int m = t >= nks ? 1 : 0, ks = t - m * nks;
-      const int slot = j % D;
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const bool ok = stage_wait<D>(full0 + 8 * slot, j, &s_abort, a, lane);
+      const bool ok = stage_wait(full0 + 8 * cslot, cphase, &s_abort, a, lane);
       if (ok) {
-        const int ng = min(I4_KS, NG - ks * I4_KS);
-        i4_task(myring + slot * I4_STAGE, ng, xfrag + (size_t)ks * I4_SLICE_KSTEPS * nb * 4, lane, nb, acc);
+        const uint8_t* st = myring + cslot * I4_STAGE;
+        const uint2* xl = xcol + ks * I4_SLICE_KSTEPS;
+        if (ks * I4_KS + 2 <= NG) i4_task<2>(st + lane * 16, st + 1024 + gq * 4, xl, acc);
+        else i4_task<1>(st + lane * 16, st + 1024 + gq * 4, xl, acc);
       }
       __syncwarp();
       ++j;
+      if (++cslot == D) {
+        cslot = 0;
+        cphase ^= 1u;
+      }
       if (ok && j_issue < nw) issue_next();   // refill the slot just read
       if (ok && p < ntok) {
         float* dst = part + ((size_t)(m * nks + ks) * I4_PMAX + p) * rows32 + rb * 32;
@@ -325,7 +348,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
   using SM = I4Smem<NW, D>;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::ring);
   uint2* xfrag = reinterpret_cast<uint2*>(smem + SM::ring + SM::bars);
-  float* vin = reinterpret_cast<float*>(smem + SM::ring + SM::bars + I4_SLICE_KSTEPS * 8 * 4 * 8);
+  float* vin = reinterpret_cast<float*>(smem + SM::ring + SM::bars + 8 * 4 * i4_kstride(I4_SLICE_KSTEPS) * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars + warp * D);
   const uint32_t ring0 = smem_u32(smem + warp * D * I4_STAGE);
@@ -362,19 +385,23 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
 
   const int first = t0 + warp;
   const int nw = first < t1 ? (t1 - first + NW - 1) / NW : 0;
-  int iu = first / ntask, irb = first - iu * ntask;   // issue cursor: unit (pass, k-slice), row block
-  int j_issue = 0;
+  // issue cursor: pass ipi, k-slice iks, row block irb (no divisions per task)
+  int ipi = first / per_pass, iks = (first - ipi * per_pass) / ntask;
+  int irb = first - ipi * per_pass - iks * ntask;
+  int j_issue = 0, islot = 0;
   auto issue_next = [&]() {
-    const int ipi = iu / nks, iks = iu - ipi * nks;
     const int ng = min(I4_KS, NG - iks * I4_KS);
     const uint8_t* src = s_rec[ipi - pi0] + rg.off[2] + ((size_t)irb * NG + (size_t)iks * I4_KS) * I4_PAIR_BLOCK;
-    const int slot = j_issue % D;
-    stage_issue(lane, full0 + 8 * slot, ring0 + slot * I4_STAGE, src, (uint32_t)ng * I4_PAIR_BLOCK);
+    stage_issue(lane, full0 + 8 * islot, ring0 + islot * I4_STAGE, src, (uint32_t)ng * I4_PAIR_BLOCK);
     ++j_issue;
+    if (++islot == D) islot = 0;
     irb += NW;
     while (irb >= ntask) {
       irb -= ntask;
-      ++iu;
+      if (++iks == nks) {
+        iks = 0;
+        ++ipi;
+      }
     }
   };
   while (j_issue < min(D, nw)) issue_next();
@@ -384,6 +411,8 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
   const int gq = lane >> 2, p = lane & 3;
   const uint8_t* myring = smem + warp * D * I4_STAGE;
   int j = 0;
+  int cslot = 0;
+  uint32_t cphase = 0u;
   int ti = first;
   for (int seg = t0; seg < t1;) {  // segments = one unit (pass, k-slice) each
     const int u = seg / ntask;
@@ -404,18 +433,20 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
         const float* pg = a.part_gu + ((size_t)pass * 2 * nks_gu * I4_PMAX + ts) * rows32_f + kbase + kk;
         const float* pu = pg + (size_t)nks_gu * stride;
         float gs = 0.f, us = 0.f;
-        for (int s0 = 0; s0 < nks_gu; s0 += 8) {
-          float gv[8], uv[8];
+        for (int s0 = 0; s0 < nks_gu; s0 += 16) {   // 32 loads in flight, added in slice order
+          float gv[16], uv[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < 16; ++q) {
             const bool in = s0 + q < nks_gu;
             gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * stride) : 0.f;
             uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * stride) : 0.f;
           }
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            gs += gv[q];
-            us += uv[q];
+          for (int q = 0; q < 16; ++q) {
+            if (s0 + q < nks_gu) {
+              gs += gv[q];
+              us += uv[q];
+            }
           }
         }
         v = gs / (1.f + expf(-gs)) * us;
@@ -427,14 +458,22 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
                  [&](int ts, int k) { return vin[ts * (I4_KS * I4_GROUP) + k]; });
     named_sync(1, nthr);
     float* dst0 = a.part_d + ((size_t)pass * nks + ks) * I4_PMAX * rows32;
+    const uint2* xcol = xfrag + i4_lane_col(lane, nb) * i4_kstride(I4_SLICE_KSTEPS);
     for (; ti < seg_end; ti += NW) {
       const int rb = ti - u * ntask;
-      const int slot = j % D;
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const bool ok = stage_wait<D>(full0 + 8 * slot, j, &s_abort, a, lane);
-      if (ok) i4_task(myring + slot * I4_STAGE, ng, xfrag, lane, nb, acc);
+      const bool ok = stage_wait(full0 + 8 * cslot, cphase, &s_abort, a, lane);
+      if (ok) {
+        const uint8_t* st = myring + cslot * I4_STAGE;
+        if (ng == 2) i4_task<2>(st + lane * 16, st + 1024 + gq * 4, xcol, acc);
+        else i4_task<1>(st + lane * 16, st + 1024 + gq * 4, xcol, acc);
+      }
       __syncwarp();
       ++j;
+      if (++cslot == D) {
+        cslot = 0;
+        cphase ^= 1u;
+      }
       if (ok && j_issue < nw) issue_next();
       if (ok && p < ntok) {
         float* dst = dst0 + (size_t)p * rows32 + rb * 32;

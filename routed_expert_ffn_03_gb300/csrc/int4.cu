@@ -499,6 +499,8 @@ struct I4Launch {
 static I4Launch i4_config(int H, int max_tokens) {
   const int nb = 2 * std::min(max_tokens, I4_PMAX);
   const size_t cap = 227 * 1024 - I4_STATIC_SMEM;
+  if ((size_t)I4Smem<24, 2>::gateup(H, nb) <= cap)
+    return {24, 2, (size_t)I4Smem<24, 2>::gateup(H, nb), (size_t)I4Smem<24, 2>::down()};
   if ((size_t)I4Smem<16, 3>::gateup(H, nb) <= cap)
     return {16, 3, (size_t)I4Smem<16, 3>::gateup(H, nb), (size_t)I4Smem<16, 3>::down()};
   if ((size_t)I4Smem<16, 2>::gateup(H, nb) <= cap)
@@ -517,6 +519,7 @@ static cudaError_t i4_attrs(const I4Launch& c) {
 
 cudaError_t int4_set_attributes(int H, int max_tokens) {
   const I4Launch c = i4_config(H, max_tokens);
+  if (c.nw == 24) return i4_attrs<24, 2>(c);
   if (c.nw == 16 && c.d == 3) return i4_attrs<16, 3>(c);
   if (c.nw == 16) return i4_attrs<16, 2>(c);
   return i4_attrs<8, 2>(c);
@@ -524,6 +527,7 @@ cudaError_t int4_set_attributes(int H, int max_tokens) {
 
 cudaError_t launch_int4_gateup(const ExpertArgs& a, int grid, cudaStream_t s) {
   const I4Launch c = i4_config(a.H, a.max_tokens);
+  if (c.nw == 24) return launch_pdl(int4_gateup_kernel<24, 2>, grid, 24 * 32, c.smem_gu, s, a);
   if (c.nw == 16 && c.d == 3) return launch_pdl(int4_gateup_kernel<16, 3>, grid, 16 * 32, c.smem_gu, s, a);
   if (c.nw == 16) return launch_pdl(int4_gateup_kernel<16, 2>, grid, 16 * 32, c.smem_gu, s, a);
   return launch_pdl(int4_gateup_kernel<8, 2>, grid, 8 * 32, c.smem_gu, s, a);
@@ -531,6 +535,7 @@ cudaError_t launch_int4_gateup(const ExpertArgs& a, int grid, cudaStream_t s) {
 
 cudaError_t launch_int4_down(const ExpertArgs& a, int grid, cudaStream_t s) {
   const I4Launch c = i4_config(a.H, a.max_tokens);
+  if (c.nw == 24) return launch_pdl(int4_down_kernel<24, 2>, grid, 24 * 32, c.smem_down, s, a);
   if (c.nw == 16 && c.d == 3) return launch_pdl(int4_down_kernel<16, 3>, grid, 16 * 32, c.smem_down, s, a);
   if (c.nw == 16) return launch_pdl(int4_down_kernel<16, 2>, grid, 16 * 32, c.smem_down, s, a);
   return launch_pdl(int4_down_kernel<8, 2>, grid, 8 * 32, c.smem_down, s, a);

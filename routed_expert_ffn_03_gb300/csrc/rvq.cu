@@ -33,11 +33,19 @@ constexpr int RV_VIN_BYTES = RVQ_KS * RVQ_GROUP * 4;   // 2048
 constexpr int RV_SMEM = RV_LUT_BYTES + RV_VIN_BYTES;
 constexpr int RV_HQ = RVQ_TASK_BYTES / 512 / 2;        // 6 uint4 per lane per half task (32 groups)
 
-// A table entry at byte offset addr + OFF of the table (an ordinary shared-memory load,
-// so it stays ordered after the barrier that ends the table build).
-template <int OFF>
-__device__ __forceinline__ float lds_f32(const float* lut, uint32_t addr) {
-  return *reinterpret_cast<const float*>(reinterpret_cast<const char*>(lut) + addr + OFF);
+// The table starts the block's dynamic shared memory.  Where that memory starts at
+// shared address RV_DYN_BASE (1024 on this part: the reserved 1 KB comes first) a lookup
+// is a single shared load [prmt result + constant]; elsewhere the base is added.
+constexpr uint32_t RV_DYN_BASE = 1024;
+
+// Table entry at shared address addr + delta + OFF (delta = 0 on the fast path).  The
+// asm is volatile with a memory clobber, so it stays after the barrier that ends the
+// table build and before the one that starts the next build.
+template <uint32_t OFF, bool FAST>
+__device__ __forceinline__ float lds_f32(uint32_t addr, uint32_t delta) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(FAST ? addr : addr + delta), "n"(OFF) : "memory");
+  return v;
 }
 
 // Half HALF (groups 32 HALF .. 32 HALF + 31 of the lane stream) of a task's codes.
@@ -54,9 +62,10 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&v)[RV_HQ], int w) {
 
 // Adds the three lookups of each of the half's 32 groups (positions i = 32 HALF + 0..31,
 // group q = lane XOR i) to the stage accumulators.
-template <int HALF>
-__device__ __forceinline__ void rvq_half_sum(const uint4 (&v)[RV_HQ], const float* lut, uint32_t l4, float& acc0,
+template <int HALF, bool FAST>
+__device__ __forceinline__ void rvq_half_sum(const uint4 (&v)[RV_HQ], uint32_t delta, uint32_t l4, float& acc0,
                                              float& acc1, float& acc2) {
+  constexpr uint32_t S0 = RV_DYN_BASE, S1 = RV_DYN_BASE + 65536, S2 = RV_DYN_BASE + 131072;
 #pragma unroll
   for (int c4 = 0; c4 < 8; ++c4) {
     const uint32_t w0 = word_of(v, 3 * c4), w1 = word_of(v, 3 * c4 + 1), w2 = word_of(v, 3 * c4 + 2);
@@ -65,19 +74,19 @@ __device__ __forceinline__ void rvq_half_sum(const uint4 (&v)[RV_HQ], const floa
     const uint32_t q1 = l4 ^ (uint32_t)((i0 + 1) << 2);
     const uint32_t q2 = l4 ^ (uint32_t)((i0 + 2) << 2);
     const uint32_t q3 = l4 ^ (uint32_t)((i0 + 3) << 2);
-    // prmt: byte 1 <- code byte, byte 0 <- qoff, bytes 2,3 <- 0  => (c << 8) | 4q
-    acc0 += lds_f32<0>(lut, prmt(w0, q0, 0x5504));
-    acc1 += lds_f32<65536>(lut, prmt(w0, q0, 0x5514));
-    acc2 += lds_f32<131072>(lut, prmt(w0, q0, 0x5524));
-    acc0 += lds_f32<0>(lut, prmt(w0, q1, 0x5534));
-    acc1 += lds_f32<65536>(lut, prmt(w1, q1, 0x5504));
-    acc2 += lds_f32<131072>(lut, prmt(w1, q1, 0x5514));
-    acc0 += lds_f32<0>(lut, prmt(w1, q2, 0x5524));
-    acc1 += lds_f32<65536>(lut, prmt(w1, q2, 0x5534));
-    acc2 += lds_f32<131072>(lut, prmt(w2, q2, 0x5504));
-    acc0 += lds_f32<0>(lut, prmt(w2, q3, 0x5514));
-    acc1 += lds_f32<65536>(lut, prmt(w2, q3, 0x5524));
-    acc2 += lds_f32<131072>(lut, prmt(w2, q3, 0x5534));
+    // prmt: byte 1 <- code byte, byte 0 <- 4q, bytes 2,3 <- 0  => (c << 8) | 4q
+    acc0 += lds_f32<S0, FAST>(prmt(w0, q0, 0x5504), delta);
+    acc1 += lds_f32<S1, FAST>(prmt(w0, q0, 0x5514), delta);
+    acc2 += lds_f32<S2, FAST>(prmt(w0, q0, 0x5524), delta);
+    acc0 += lds_f32<S0, FAST>(prmt(w0, q1, 0x5534), delta);
+    acc1 += lds_f32<S1, FAST>(prmt(w1, q1, 0x5504), delta);
+    acc2 += lds_f32<S2, FAST>(prmt(w1, q1, 0x5514), delta);
+    acc0 += lds_f32<S0, FAST>(prmt(w1, q2, 0x5524), delta);
+    acc1 += lds_f32<S1, FAST>(prmt(w1, q2, 0x5534), delta);
+    acc2 += lds_f32<S2, FAST>(prmt(w2, q2, 0x5504), delta);
+    acc0 += lds_f32<S0, FAST>(prmt(w2, q3, 0x5514), delta);
+    acc1 += lds_f32<S1, FAST>(prmt(w2, q3, 0x5524), delta);
+    acc2 += lds_f32<S2, FAST>(prmt(w2, q3, 0x5534), delta);
   }
 }
 
@@ -121,6 +130,7 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   const int t0 = (int)((long long)total * blockIdx.x / gridDim.x);
   const int t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
   const uint32_t l4 = (uint32_t)lane << 2;
+  const uint32_t delta = smem_u32(smem) - RV_DYN_BASE;   // 0 on the fast path
 
   for (int i = t0; i < t1;) {
     const int u = i / ntask;
@@ -185,6 +195,9 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
         }
       }
       const uint32_t* cb = reinterpret_cast<const uint32_t*>(U.base);  // fp16 [768][8]
+      int jofs[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) jofs[r] = 8 * ((p + r) & 3);
       for (int nt = warp; nt < 96; nt += RV_NW) {
         const int e0 = nt * 8;
         const uint32_t b = __ldg(cb + (e0 + gq) * 4 + p);
@@ -195,16 +208,26 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
           mma_1688(dA, alo[2 * P][0], alo[2 * P][1], b);
           mma_1688(dB, ahi[2 * P + 1][0], ahi[2 * P + 1][1], b);
           mma_1688(dB, alo[2 * P + 1][0], alo[2 * P + 1][1], b);
-          // value j of entry e: q = 32P + g + 8j  (j: A row g, A row g+8, B row g, B row g+8)
+          // value j of entry e: q = 32P + g + 8j  (j: A row g, A row g+8, B row g, B row g+8).
+          // Store r writes value j = (p + r) & 3, so one store touches 32 banks: the values
+          // are rotated left by p with two conditional swaps instead of indexed selects.
+          float v0[4] = {dA[0], dA[2], dB[0], dB[2]}, v1[4] = {dA[1], dA[3], dB[1], dB[3]};
+          if (p & 1) {
+            const float t0 = v0[0], t1 = v1[0];
+            v0[0] = v0[1]; v0[1] = v0[2]; v0[2] = v0[3]; v0[3] = t0;
+            v1[0] = v1[1]; v1[1] = v1[2]; v1[2] = v1[3]; v1[3] = t1;
+          }
+          if (p & 2) {
+            float t = v0[0]; v0[0] = v0[2]; v0[2] = t;
+            t = v0[1]; v0[1] = v0[3]; v0[3] = t;
+            t = v1[0]; v1[0] = v1[2]; v1[2] = t;
+            t = v1[1]; v1[1] = v1[3]; v1[3] = t;
+          }
           float* row0 = lutf + (size_t)(e0 + 2 * p) * RVQ_KS + 32 * P + gq;
-          float* row1 = row0 + RVQ_KS;
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
-            const int j = (p + r) & 3;
-            const float v0 = j == 0 ? dA[0] : j == 1 ? dA[2] : j == 2 ? dB[0] : dB[2];
-            const float v1 = j == 0 ? dA[1] : j == 1 ? dA[3] : j == 2 ? dB[1] : dB[3];
-            row0[8 * j] = v0;
-            row1[8 * j] = v1;
+            row0[jofs[r]] = v0[r];
+            row0[jofs[r] + RVQ_KS] = v1[r];
           }
         }
       }
@@ -214,16 +237,30 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
     // tasks of this unit: warp-strided; half tasks double-buffered in registers
     float* outp = (DOWN ? a.part_d + ((size_t)U.pass * nks + U.ks) * rows32
                         : a.part_gu + ((size_t)(U.pass * 2 + U.m) * nks + U.ks) * rows32);
-    while (ti < seg_end) {
-      const uint8_t* task = codes + (size_t)(ti - useg) * RVQ_TASK_BYTES;
-      load_half<1>(hb, task, lane);
-      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f;
-      rvq_half_sum<0>(ha, lutf, l4, acc0, acc1, acc2);
-      const int tn = ti + RV_NW;
-      if (tn < seg_end) load_half<0>(ha, codes + (size_t)(tn - useg) * RVQ_TASK_BYTES, lane);
-      rvq_half_sum<1>(hb, lutf, l4, acc0, acc1, acc2);
-      outp[(size_t)(ti - useg) * 32 + lane] = (acc0 + acc1) + acc2;
-      ti = tn;
+    if (delta == 0u) {
+      while (ti < seg_end) {
+        const uint8_t* task = codes + (size_t)(ti - useg) * RVQ_TASK_BYTES;
+        load_half<1>(hb, task, lane);
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f;
+        rvq_half_sum<0, true>(ha, 0u, l4, acc0, acc1, acc2);
+        const int tn = ti + RV_NW;
+        if (tn < seg_end) load_half<0>(ha, codes + (size_t)(tn - useg) * RVQ_TASK_BYTES, lane);
+        rvq_half_sum<1, true>(hb, 0u, l4, acc0, acc1, acc2);
+        outp[(size_t)(ti - useg) * 32 + lane] = (acc0 + acc1) + acc2;
+        ti = tn;
+      }
+    } else {
+      while (ti < seg_end) {
+        const uint8_t* task = codes + (size_t)(ti - useg) * RVQ_TASK_BYTES;
+        load_half<1>(hb, task, lane);
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f;
+        rvq_half_sum<0, false>(ha, delta, l4, acc0, acc1, acc2);
+        const int tn = ti + RV_NW;
+        if (tn < seg_end) load_half<0>(ha, codes + (size_t)(tn - useg) * RVQ_TASK_BYTES, lane);
+        rvq_half_sum<1, false>(hb, delta, l4, acc0, acc1, acc2);
+        outp[(size_t)(ti - useg) * 32 + lane] = (acc0 + acc1) + acc2;
+        ti = tn;
+      }
     }
     i = seg_end;
   }

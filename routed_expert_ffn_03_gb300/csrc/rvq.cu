@@ -27,7 +27,7 @@
 
 namespace moe {
 
-constexpr int RV_NW = 16;                              // warps per block
+constexpr int RV_NW = 16;                              // warps per block (divides 96)
 constexpr int RV_LUT_BYTES = 3 * 256 * RVQ_KS * 4;     // 196608
 constexpr int RV_VIN_BYTES = RVQ_KS * RVQ_GROUP * 4;   // 2048
 constexpr int RV_SMEM = RV_LUT_BYTES + RV_VIN_BYTES;
@@ -144,6 +144,15 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
     uint4 ha[RV_HQ], hb[RV_HQ];
     if (ti < seg_end) load_half<0>(ha, codes + (size_t)(ti - useg) * RVQ_TASK_BYTES, lane);
 
+    // this warp's codebook fragments (6 n-tiles of 8 entries) go in flight now as well
+    constexpr int RV_NT = 96 / RV_NW;
+    uint32_t bfr[RV_NT];
+    {
+      const uint32_t* cb = reinterpret_cast<const uint32_t*>(U.base);  // fp16 [768][8]
+#pragma unroll
+      for (int n = 0; n < RV_NT; ++n) bfr[n] = __ldg(cb + ((warp + n * RV_NW) * 8 + gq) * 4 + p);
+    }
+
     __syncthreads();  // the previous unit's table is no longer read
     {
       const int tok = __ldcg(a.plan.pass_tok + U.pass);   // one token per pass
@@ -194,13 +203,13 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
           alo[mt][h] = pack_half2(l0, l1);
         }
       }
-      const uint32_t* cb = reinterpret_cast<const uint32_t*>(U.base);  // fp16 [768][8]
       int jofs[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) jofs[r] = 8 * ((p + r) & 3);
-      for (int nt = warp; nt < 96; nt += RV_NW) {
-        const int e0 = nt * 8;
-        const uint32_t b = __ldg(cb + (e0 + gq) * 4 + p);
+#pragma unroll
+      for (int n = 0; n < RV_NT; ++n) {
+        const int e0 = (warp + n * RV_NW) * 8;
+        const uint32_t b = bfr[n];
 #pragma unroll
         for (int P = 0; P < 2; ++P) {
           float dA[4] = {0.f, 0.f, 0.f, 0.f}, dB[4] = {0.f, 0.f, 0.f, 0.f};

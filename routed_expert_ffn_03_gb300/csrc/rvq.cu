@@ -124,6 +124,15 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   const MatGeom gg = rg.m[0];
   const int nks = g.nks, ntask = g.ntask;
   const int rows32 = ntask * 32, rows32_gu = gg.ntask * 32;
+  // gate/up waits for the router (plan, x) at once.  down reads only the plan, which is
+  // older than the gate/up kernel (that kernel waited for it before letting this one
+  // start), and the weights before it waits, so its first codes and codebooks are in
+  // flight while gate/up finishes; the gate/up partials are read after the wait.
+  if (!DOWN) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
+  bool waited = !DOWN;
   const int p_begin = a.range.p_begin;
   const int p_end = a.range.p_end >= 0 ? a.range.p_end : __ldcg(a.range.count ? a.range.count : &a.plan.hdr->n_pass);
   const int total = max(0, p_end - p_begin) * mats * nks * ntask;
@@ -132,6 +141,10 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   const uint32_t l4 = (uint32_t)lane << 2;
   const uint32_t delta = smem_u32(smem) - RV_DYN_BASE;   // 0 on the fast path
 
+  if (t0 >= t1 && !waited) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   for (int i = t0; i < t1;) {
     const int u = i / ntask;
     const int seg_end = min(t1, (u + 1) * ntask);
@@ -153,6 +166,11 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
       for (int n = 0; n < RV_NT; ++n) bfr[n] = __ldg(cb + ((warp + n * RV_NW) * 8 + gq) * 4 + p);
     }
 
+    if (!waited) {
+      pdl_wait();
+      pdl_launch_dependents();
+      waited = true;
+    }
     __syncthreads();  // the previous unit's table is no longer read
     {
       const int tok = __ldcg(a.plan.pass_tok + U.pass);   // one token per pass
@@ -282,12 +300,10 @@ cudaError_t rvq_set_attributes() {
 }
 
 cudaError_t launch_rvq_gateup(const ExpertArgs& a, int grid, cudaStream_t s) {
-  rvq_kernel<false><<<grid, RV_NW * 32, RV_SMEM, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(rvq_kernel<false>, grid, RV_NW * 32, RV_SMEM, s, a);
 }
 cudaError_t launch_rvq_down(const ExpertArgs& a, int grid, cudaStream_t s) {
-  rvq_kernel<true><<<grid, RV_NW * 32, RV_SMEM, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(rvq_kernel<true>, grid, RV_NW * 32, RV_SMEM, s, a);
 }
 
 }  // namespace moe

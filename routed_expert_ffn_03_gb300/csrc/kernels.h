@@ -19,7 +19,7 @@ struct DevCounters {           // updated on the device by the router's last blo
   unsigned long long forwards, tokens, lookups, bytes_touched, bytes_router;
 };
 
-constexpr int ROUTER_FUSED_MAXT = 8;   // tokens of a fused stack step (norm inside the router)
+constexpr int ROUTER_FUSED_MAXT = 4;   // tokens of a fused stack step (norm inside the router)
 
 struct RouterArgs {
   const uint16_t* x;     // bf16 [T][H] router input (when xres is null)

@@ -52,7 +52,76 @@ __device__ __forceinline__ int big_chunks(int c, int big_min) {
   return (big_min > 0 && c >= big_min) ? cdiv(c, GEMM_MAX_TOKENS) : 0;
 }
 
-__global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
+// Top-k of one token's E logits (one warp; NV * 32 >= E values, lane l holds experts
+// l + 32 i), then the k weights; writes the plan's and the per-layer copy of the routing.
+// Each lane keeps the maximum of its own experts not yet taken; the warp takes the best k
+// times, and only the lane that gave its maximum away looks for its next one.  NaN ranks
+// as -inf; equal values rank the lower id first.
+template <int NV>
+__device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src, bool global_src, int t, int lane,
+                                           int* s_idx) {
+  const int E = a.E, k = a.k;
+  float v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int ee = lane + 32 * i;
+    v[i] = ee < E ? (global_src ? __ldcg(src + ee) : src[ee]) : -INFINITY;
+  }
+  uint32_t taken = 0u;
+  auto lane_best = [&](float& bv, int& be) {
+    bv = -INFINITY;
+    be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int ee = lane + 32 * i;
+      const float x = v[i] != v[i] ? -INFINITY : v[i];
+      if (ee < E && !((taken >> i) & 1u) && (x > bv || (x == bv && ee < be))) { bv = x; be = ee; }
+    }
+  };
+  float lv;
+  int le;
+  lane_best(lv, le);
+  int my_e = 0;
+  float my_l = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = lv;
+    int be = le;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    }
+    if (lane == j) { my_e = be; my_l = bv; }
+    if (be == le) {   // this lane's maximum was taken (ids are distinct across lanes)
+      taken |= 1u << ((be - lane) >> 5);
+      lane_best(lv, le);
+    }
+  }
+  // weights over the k selected (rank order = lane order)
+  const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+  float num = 0.f;
+  if (lane < k) {
+    if (a.kind == 0) num = expf(my_l - lmax);
+    else num = 1.f / (1.f + expf(-my_l));
+  }
+  float den = num;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (lane < k) {
+    const float w = num / den;
+    a.plan.idx[t * k + lane] = my_e;
+    a.plan.w[t * k + lane] = w;
+    a.store_idx[t * k + lane] = my_e;
+    a.store_w[t * k + lane] = w;
+    s_idx[t * k + lane] = my_e;
+  }
+}
+
+// MINB = blocks per SM the registers must allow: 3 where the grid is larger than two
+// blocks per SM (so it still runs in one wave), else 1 (no register cap).
+template <int MINB>
+__global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
   extern __shared__ __align__(16) int sm[];
   __shared__ float s_inv[ROUTER_FUSED_MAXT];
   __shared__ float s_red[32];
@@ -219,64 +288,11 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 
   // ---------------- phase 2a: top-k per token (one warp per token)
   for (int t = warp; t < T; t += nwarps) {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int ee = lane + 32 * i;
-      v[i] = ee < E ? (two_level ? __ldcg(logits + (size_t)t * E + ee) : slog[t * E + ee]) : -INFINITY;
-    }
-    // each lane keeps the maximum of its own experts not yet taken; the warp takes the
-    // best k times, and only the lane that gave its maximum away looks for its next one.
-    // NaN ranks as -inf; equal values rank the lower id first.
-    uint32_t taken = 0u;
-    auto lane_best = [&](float& bv, int& be) {
-      bv = -INFINITY;
-      be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int ee = lane + 32 * i;
-        const float x = v[i] != v[i] ? -INFINITY : v[i];
-        if (ee < E && !((taken >> i) & 1u) && (x > bv || (x == bv && ee < be))) { bv = x; be = ee; }
-      }
-    };
-    float lv;
-    int le;
-    lane_best(lv, le);
-    int my_e = 0;
-    float my_l = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = lv;
-      int be = le;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      if (lane == j) { my_e = be; my_l = bv; }
-      if (be == le) {   // this lane's maximum was taken (ids are distinct across lanes)
-        taken |= 1u << ((be - lane) >> 5);
-        lane_best(lv, le);
-      }
-    }
-    // weights over the k selected (rank order = lane order)
-    const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-    float num = 0.f;
-    if (lane < k) {
-      if (a.kind == 0) num = expf(my_l - lmax);
-      else num = 1.f / (1.f + expf(-my_l));
-    }
-    float den = num;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (lane < k) {
-      const float w = num / den;
-      a.plan.idx[t * k + lane] = my_e;
-      a.plan.w[t * k + lane] = w;
-      a.store_idx[t * k + lane] = my_e;
-      a.store_w[t * k + lane] = w;
-      s_idx[t * k + lane] = my_e;
-    }
+    const float* src = two_level ? logits + (size_t)t * E : slog + t * E;
+    if (E <= 128) topk_token<4>(a, src, two_level, t, lane, s_idx);
+    else if (E <= 256) topk_token<8>(a, src, two_level, t, lane, s_idx);
+    else if (E <= 512) topk_token<16>(a, src, two_level, t, lane, s_idx);
+    else topk_token<32>(a, src, two_level, t, lane, s_idx);
   }
   __syncthreads();
 
@@ -415,8 +431,9 @@ __global__ void __launch_bounds__(256) router_kernel(RouterArgs a) {
 }
 
 cudaError_t router_set_attributes() {
-  return cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              160 * 1024);
+  cudaError_t e = cudaFuncSetAttribute(router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(router_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
 }
 
 size_t router_smem_bytes(int H, int T, int E, int k) {
@@ -426,9 +443,10 @@ size_t router_smem_bytes(int H, int T, int E, int k) {
 }
 
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s) {
-  (void)num_sms;
   const int grid = cdiv(a.H, RSW) * cdiv(a.E, REPB);
-  return launch_pdl(router_kernel, grid, 256, router_smem_bytes(a.H, a.T, a.E, a.k), s, a);
+  const size_t smem = router_smem_bytes(a.H, a.T, a.E, a.k);
+  if (grid > 2 * num_sms) return launch_pdl(router_kernel<3>, grid, 256, smem, s, a);
+  return launch_pdl(router_kernel<1>, grid, 256, smem, s, a);
 }
 
 }  // namespace moe

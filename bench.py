@@ -285,6 +285,8 @@ def run_gpu(args, cfg, rank, world, device):
     xn = torch.zeros((T, H), dtype=torch.int16, device=device)
     stream = torch.cuda.Stream(device=device)
     streamed = cfg["cache"] != 0
+    if streamed:
+        ctx.set_readahead(bool(args.readahead))
 
     def layers():
         # x += y_prev; xn = rmsnorm(x); y = layer(xn)   (fused stack step), then the last add
@@ -428,12 +430,18 @@ def run_gpu(args, cfg, rank, world, device):
         miss_gbs = st["bytes_h2d"] / max(1e-9, st["h2d_ms"] / 1e3) / 1e9 if st["h2d_ms"] else None
         out["hit_series_per64"] = hit_series
         out["streaming"] = {
+            "readahead": bool(args.readahead),
             "misses_per_token": round(st["misses"] / max(1, K), 2), "hits": st["hits"], "misses": st["misses"],
-            "bytes_h2d": st["bytes_h2d"], "copy_span_ms": round(st["h2d_ms"], 2),
+            "prefetches": st["prefetches"], "prefetch_hits": st["prefetch_hits"],
+            "prefetch_accuracy": round(st["prefetch_hits"] / st["prefetches"], 4) if st["prefetches"] else None,
+            "bytes_h2d": st["bytes_h2d"], "link_busy_ms": round(st["h2d_ms"], 2),
+            "link_busy_frac_of_run": round(st["h2d_ms"] / ms, 4),
             "miss_copy_gbs": round(miss_gbs, 2) if miss_gbs else None,
             "link_gbs_measured": round(link, 2),
             "miss_frac_of_link": round(miss_gbs / link, 4) if miss_gbs else None,
-            "link_measure": "pinned 1 GiB cudaMemcpyAsync host->device, best of 10, same run",
+            "link_measure": "pinned 1 GiB cudaMemcpyAsync host->device, best of 10, same run; copy GB/s = all "
+                            "expert bytes copied (misses and read-ahead) / time the link was busy (union of the "
+                            "copy batches)",
             "cache_slots": st["cache_slots"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ctx.close()
@@ -520,6 +528,8 @@ def main():
     ap.add_argument("--tokens-per-step", type=int, default=0, help="override T (dsv3: 1, 4, 32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prof-steps", type=int, default=16, help="replays of the per-kernel event graph")
+    ap.add_argument("--readahead", type=int, default=1, choices=[0, 1],
+                    help="streamed configs: predict the next layer's experts and copy them early")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

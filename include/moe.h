@@ -110,8 +110,13 @@ typedef struct {
     unsigned long long bytes_h2d;             /* expert bytes copied host -> device */
     unsigned long long record_bytes;          /* kernel-layout bytes of one expert */
     unsigned long long cache_slots;           /* HBM expert slots (0 when all resident) */
-    double h2d_ms;                            /* summed span of the miss copies of each forward,
-                                                 first copy start to last copy end (streamed) */
+    double h2d_ms;                            /* time the host->device link was busy with expert
+                                                 copies: the union over copy batches (one
+                                                 forward's misses, or one read-ahead) of first
+                                                 copy start to last copy end (streamed) */
+    unsigned long long prefetches;            /* records copied by read-ahead (streamed) */
+    unsigned long long prefetch_hits;         /* lookups that found a record read-ahead put there
+                                                 and no lookup had used yet */
 } moe_stats_t;
 
 typedef struct moe_ctx moe_ctx;
@@ -174,6 +179,19 @@ moe_status moe_residual_rmsnorm(moe_ctx* ctx, float* x, const float* y, uint16_t
  * (it synchronises the context's device). */
 moe_status moe_stats(moe_ctx* ctx, moe_stats_t* out);
 moe_status moe_reset_stats(moe_ctx* ctx);
+
+/* Read-ahead (streamed contexts; "Introducing WARP", section How WARP keeps the model out
+ * of RAM: predict the next layer's experts and start loading them early).  With enable = 1,
+ * every moe_forward / moe_forward_residual of layer l < num_layers - 1 ends by applying
+ * layer l+1's router to layer l's router input (bf16 xn) with its own scratch, reading the
+ * predicted experts back (the host waits for that small router only), and queuing copies
+ * of the predicted experts that are not cached into least-recently-used unpinned slots,
+ * behind layer l's miss copies.  The next forward finds them as hits; its kernels for such
+ * an expert wait for that copy.  Results are bit-identical with and without read-ahead;
+ * a wrong prediction only costs link time.  Meant for callers that run the layers in
+ * order.  enable = 0 turns it off (the default).  MOE_EINVAL for enable outside {0, 1}, or
+ * enable = 1 on a context with every expert resident. */
+moe_status moe_set_readahead(moe_ctx* ctx, int enable);
 
 /* Release everything the context owns.  Safe on NULL. */
 moe_status moe_destroy(moe_ctx* ctx);

@@ -122,9 +122,33 @@ struct moe_ctx {
   static constexpr int kCopyStreams = 4;
   cudaStream_t side[kCopyStreams] = {}, reg = nullptr;
   std::vector<cudaEvent_t> copy_ev;
-  cudaEvent_t h2d_t0 = nullptr, h2d_t1[kCopyStreams] = {};
-  bool h2d_pending = false;
-  int h2d_streams_used = 0;
+  // link accounting: each batch of copies (one forward's misses, or one read-ahead) is the
+  // interval from its first copy's start to its last copy's end, timed against ref_ev; the
+  // busy time is the union of the intervals, merged in issue order
+  static constexpr int kBatches = 8;
+  struct CopyBatch {
+    cudaEvent_t t0 = nullptr, t1[kCopyStreams] = {};
+    int ns = 0;
+  } batch[kBatches];
+  int batch_head = 0, batch_count = 0;  // ring of batches not yet accounted
+  cudaEvent_t ref_ev = nullptr;
+  double busy_end_ms = -1.0;
+
+  // read-ahead (streamed): the next layer's experts predicted from this layer's router input
+  int readahead = 0;
+  cudaStream_t pred = nullptr;
+  float* d_rpart2 = nullptr;
+  unsigned int* d_ticket2 = nullptr;
+  void* d_plan_mem2 = nullptr;
+  PlanPtrs plan2{};
+  DevCounters* d_counters2 = nullptr;
+  int* d_pstore_idx = nullptr;
+  float* d_pstore_w = nullptr;
+  int* h_rb2 = nullptr;                 // pinned readback: hdr(4) | pad | uniq[E]
+  std::vector<cudaEvent_t> slot_ev;     // [slot] end of the last read-ahead copy into it
+  std::vector<char> slot_inflight;      // that copy may still be running
+  std::vector<char> slot_prefetched;    // filled by read-ahead and not looked up since
+  unsigned long long prefetches = 0, prefetch_hits = 0;
   uint8_t* d_blob_stage = nullptr;
   uint8_t* d_rec_stage = nullptr;
 
@@ -199,9 +223,21 @@ void free_all(moe_ctx* c) {
   cudaFree(c->d_counters);
   if (c->h_rb) cudaFreeHost(c->h_rb);
   for (auto ev : c->copy_ev) cudaEventDestroy(ev);
-  if (c->h2d_t0) cudaEventDestroy(c->h2d_t0);
-  for (auto ev : c->h2d_t1)
-    if (ev) cudaEventDestroy(ev);
+  for (auto& b : c->batch) {
+    if (b.t0) cudaEventDestroy(b.t0);
+    for (auto ev : b.t1)
+      if (ev) cudaEventDestroy(ev);
+  }
+  if (c->ref_ev) cudaEventDestroy(c->ref_ev);
+  for (auto ev : c->slot_ev) cudaEventDestroy(ev);
+  if (c->pred) cudaStreamDestroy(c->pred);
+  cudaFree(c->d_rpart2);
+  cudaFree(c->d_ticket2);
+  cudaFree(c->d_plan_mem2);
+  cudaFree(c->d_counters2);
+  cudaFree(c->d_pstore_idx);
+  cudaFree(c->d_pstore_w);
+  if (c->h_rb2) cudaFreeHost(c->h_rb2);
   for (auto ev : c->prof_ev) cudaEventDestroy(ev);
   for (auto st : c->side)
     if (st) cudaStreamDestroy(st);
@@ -379,8 +415,15 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     c->slot_pinned.assign(c->n_slots, 0);
     c->copy_ev.resize(E);
     for (auto& ev : c->copy_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-    cudaEventCreate(&c->h2d_t0);
-    for (auto& ev : c->h2d_t1) cudaEventCreate(&ev);
+    for (auto& b : c->batch) {
+      cudaEventCreate(&b.t0);
+      for (auto& ev : b.t1) cudaEventCreate(&ev);
+    }
+    cudaEventCreate(&c->ref_ev);
+    c->slot_ev.resize(c->n_slots);
+    for (auto& ev : c->slot_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    c->slot_inflight.assign(c->n_slots, 0);
+    c->slot_prefetched.assign(c->n_slots, 0);
   }
   if (cudaHostAlloc((void**)&c->h_rb, (size_t)(8 + E + c->max_pass) * sizeof(int),
                     cudaHostAllocDefault) != cudaSuccess) {
@@ -423,6 +466,36 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     c->plan.big = p; p += (size_t)c->max_big * 3;
     c->plan.small_order = p; p += c->max_pass;
   }
+  if (c->streamed) {
+    // read-ahead: a second router scratch and plan, so a prediction never touches the real plan
+    AL(c->d_rpart2, rpart * sizeof(float));
+    AL(c->d_ticket2, router_tickets(E) * sizeof(unsigned int));
+    AL(c->d_counters2, sizeof(DevCounters));
+    AL(c->d_pstore_idx, (size_t)maxT * k * sizeof(int));
+    AL(c->d_pstore_w, (size_t)maxT * k * sizeof(float));
+    const size_t n_int = 16 + (size_t)c->max_pass * (2 + c->pmax) + (size_t)maxT * k * 4 + (size_t)maxT * 2 + E;
+    AL(c->d_plan_mem2, n_int * sizeof(int));
+    int* p = (int*)c->d_plan_mem2;
+    c->plan2.hdr = (Plan*)p;
+    p += 16;
+    c->plan2.pass_expert = p; p += c->max_pass;
+    c->plan2.pass_ntok = p; p += c->max_pass;
+    c->plan2.pass_tok = p; p += (size_t)c->max_pass * c->pmax;
+    c->plan2.pair_pass = p; p += (size_t)maxT * k;
+    c->plan2.pair_slot = p; p += (size_t)maxT * k;
+    c->plan2.idx = p; p += (size_t)maxT * k;
+    c->plan2.w = (float*)p; p += (size_t)maxT * k;
+    c->plan2.shared_pass = p; p += maxT;
+    c->plan2.shared_slot = p; p += maxT;
+    c->plan2.uniq = p;
+    if (cudaHostAlloc((void**)&c->h_rb2, (size_t)(8 + E) * sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      free_all(c);
+      delete c;
+      return MOE_ENOMEM;
+    }
+    cudaMemset(c->d_ticket2, 0, router_tickets(E) * sizeof(unsigned int));
+  }
 #undef AL
   cudaMemset(c->d_ticket, 0, router_tickets(E) * sizeof(unsigned int));
   cudaMemset(c->d_status, 0, 4);
@@ -430,6 +503,10 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   cudaMemset(c->d_plan_mem, 0, 16 * sizeof(int));
   bool streams_ok = cudaStreamCreateWithFlags(&c->reg, cudaStreamNonBlocking) == cudaSuccess;
   for (auto& st : c->side) streams_ok = streams_ok && cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
+  if (c->streamed) {
+    streams_ok = streams_ok && cudaStreamCreateWithFlags(&c->pred, cudaStreamNonBlocking) == cudaSuccess;
+    streams_ok = streams_ok && cudaEventRecord(c->ref_ev, c->side[0]) == cudaSuccess;
+  }
   if (!streams_ok ||
       router_set_attributes() != cudaSuccess || int4_set_attributes(H, maxT) != cudaSuccess ||
       rvq_set_attributes() != cudaSuccess || rvq_gemm_set_attributes() != cudaSuccess ||
@@ -578,6 +655,133 @@ static int cache_get(moe_ctx* c, long long key, bool* hit) {
   return s;
 }
 
+// Forget what a slot holds (its content is unknown after a failed copy).
+static void forget_slot(moe_ctx* c, int slot) {
+  if (c->slot_key[slot] >= 0) c->where.erase(c->slot_key[slot]);
+  c->slot_key[slot] = -1;
+  if (c->slot_in_lru[slot]) {
+    c->lru.erase(c->lru_it[slot]);
+    c->slot_in_lru[slot] = 0;
+  }
+  c->slot_prefetched[slot] = 0;
+}
+
+// ---------------------------------------------------------------- link accounting
+static void batch_drain(moe_ctx* c, bool wait);
+
+// A batch of copies runs on the first ns side streams: t0 on side[0], the others wait for it.
+static moe_status batch_begin(moe_ctx* c, int ns, int* idx) {
+  if (c->batch_count == moe_ctx::kBatches) batch_drain(c, true);
+  const int i = (c->batch_head + c->batch_count) % moe_ctx::kBatches;
+  moe_ctx::CopyBatch& b = c->batch[i];
+  CK(cudaEventRecord(b.t0, c->side[0]));
+  for (int q = 1; q < ns; ++q) CK(cudaStreamWaitEvent(c->side[q], b.t0, 0));
+  b.ns = ns;
+  *idx = i;
+  return MOE_OK;
+}
+
+static moe_status batch_end(moe_ctx* c, int i) {
+  moe_ctx::CopyBatch& b = c->batch[i];
+  for (int q = 0; q < b.ns; ++q) CK(cudaEventRecord(b.t1[q], c->side[q]));
+  ++c->batch_count;
+  return MOE_OK;
+}
+
+// Add the finished batches, oldest first, to the link's busy time: each is the interval
+// [t0, max t1] against ref_ev, merged with the intervals before it.  wait: wait for all.
+// When none is left pending the reference moves to now, which keeps the times short.
+static void batch_drain(moe_ctx* c, bool wait) {
+  while (c->batch_count > 0) {
+    moe_ctx::CopyBatch& b = c->batch[c->batch_head];
+    bool done = true;
+    for (int q = 0; q < b.ns && done; ++q) {
+      const cudaError_t e = wait ? cudaEventSynchronize(b.t1[q]) : cudaEventQuery(b.t1[q]);
+      if (e != cudaSuccess) done = false;
+    }
+    cudaGetLastError();
+    if (!done) return;
+    float t0 = 0.f, t1 = 0.f;
+    if (cudaEventElapsedTime(&t0, c->ref_ev, b.t0) == cudaSuccess) {
+      t1 = t0;
+      for (int q = 0; q < b.ns; ++q) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, c->ref_ev, b.t1[q]) == cudaSuccess && ms > t1) t1 = ms;
+      }
+      const double start = std::max((double)t0, c->busy_end_ms);
+      if (t1 > start) c->h2d_ms += t1 - start;
+      c->busy_end_ms = std::max(c->busy_end_ms, (double)t1);
+    }
+    cudaGetLastError();
+    c->batch_head = (c->batch_head + 1) % moe_ctx::kBatches;
+    --c->batch_count;
+  }
+  if (cudaEventRecord(c->ref_ev, c->side[0]) == cudaSuccess) c->busy_end_ms = 0.0;
+  cudaGetLastError();
+}
+
+// Read-ahead: route layer nl on this forward's router input x (bf16 on the device, written
+// before the plan read-back this forward waited for) with the prediction scratch, and
+// start copying the predicted experts that are not cached into unpinned slots, behind
+// this forward's miss copies.  Only timing depends on it: a slot's kernels always wait
+// for the copy that filled it.
+static moe_status readahead(moe_ctx* c, int nl, const void* x, int T) {
+  const int E = c->cfg.num_experts, H = c->cfg.hidden;
+  RouterArgs ra{};
+  ra.x = (const uint16_t*)x;
+  ra.W = c->d_router + (size_t)nl * E * H;
+  ra.T = T;
+  ra.H = H;
+  ra.E = E;
+  ra.k = c->cfg.top_k;
+  ra.kind = c->cfg.router;
+  ra.pmax = c->pmax;
+  ra.has_shared = 0;
+  ra.partial = c->d_rpart2;
+  ra.ticket = c->d_ticket2;
+  ra.plan = c->plan2;
+  ra.store_idx = c->d_pstore_idx;
+  ra.store_w = c->d_pstore_w;
+  ra.counters = c->d_counters2;
+  ra.record_bytes = 0;
+  ra.big_min = 0;
+  CK(launch_router(ra, c->num_sms, c->pred));
+  CK(cudaMemcpyAsync(c->h_rb2, c->plan2.hdr, 4 * sizeof(int), cudaMemcpyDeviceToHost, c->pred));
+  CK(cudaMemcpyAsync(c->h_rb2 + 8, c->plan2.uniq, (size_t)E * sizeof(int), cudaMemcpyDeviceToHost, c->pred));
+  CK(cudaStreamSynchronize(c->pred));
+  std::vector<int> todo;
+  const int n_uniq = c->h_rb2[1];
+  for (int i = 0; i < n_uniq && i < E; ++i) {
+    const int e = c->h_rb2[8 + i];
+    if (e >= 0 && e < E && !c->where.count((long long)nl * E + e)) todo.push_back(e);
+  }
+  if (todo.empty()) return MOE_OK;
+  const int ns = (int)std::min<size_t>(moe_ctx::kCopyStreams, todo.size());
+  int bi = -1;
+  moe_status bs = batch_begin(c, ns, &bi);
+  if (bs != MOE_OK) return bs;
+  for (size_t m = 0; m < todo.size(); ++m) {
+    const int e = todo[m];
+    bool hit = false;
+    const int slot = cache_get(c, (long long)nl * E + e, &hit);  // evicts an unpinned slot
+    if (slot < 0) break;
+    cudaStream_t cs = c->side[m % ns];
+    if (c->slot_inflight[slot]) CK(cudaStreamWaitEvent(cs, c->slot_ev[slot], 0));
+    const uint8_t* src = c->h_pool + ((size_t)nl * E + e) * c->rec_bytes;
+    if (cudaMemcpyAsync(c->d_slab + (size_t)slot * c->rec_bytes, src, c->rec_bytes, cudaMemcpyHostToDevice, cs) !=
+        cudaSuccess) {
+      forget_slot(c, slot);
+      return cuda_fail(c);
+    }
+    CK(cudaEventRecord(c->slot_ev[slot], cs));
+    c->slot_inflight[slot] = 1;
+    c->slot_prefetched[slot] = 1;
+    ++c->prefetches;
+    c->bytes_h2d += c->rec_bytes;
+  }
+  return batch_end(c, bi);
+}
+
 // Router input: xn (bf16) when xres is null; else the fused stack step on the residual
 // xres (+ yprev), which writes xres and xn_out.
 static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres, const float* yprev,
@@ -672,23 +876,15 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
       return c->sticky;
     }
   }
-  if (c->h2d_pending) {  // the previous forward's copies are complete: add their span
-    float span = 0.f;
-    for (int q = 0; q < c->h2d_streams_used; ++q) {
-      float ms = 0.f;
-      if (cudaEventElapsedTime(&ms, c->h2d_t0, c->h2d_t1[q]) == cudaSuccess && ms > span) span = ms;
-      cudaGetLastError();
-    }
-    c->h2d_ms += span;
-    c->h2d_pending = false;
-  }
+  batch_drain(c, false);
   const int n_pass = rb[0], n_uniq = rb[1], n_routed = rb[2];
   const int* uniq = rb + 8;
   const int* pexp = rb + 8 + E;
 
+  // lookups: hits, hits whose read-ahead copy may still be running, misses
   for (size_t i = 0; i < c->n_slots; ++i) c->slot_pinned[i] = 0;
-  std::vector<int> miss_experts;
-  std::vector<char> is_miss(E, 0);
+  std::vector<int> miss_experts, miss_slot, wait_experts, wait_slot;
+  std::vector<char> grouped(E, 0);
   for (int i = 0; i < n_uniq; ++i) {
     const int e = uniq[i];
     bool hit = false;
@@ -698,24 +894,62 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     c->h_table[e] = c->d_slab + (size_t)slot * c->rec_bytes;
     if (hit) {
       ++c->hits;
+      if (c->slot_prefetched[slot]) {
+        ++c->prefetch_hits;
+        c->slot_prefetched[slot] = 0;
+      }
+      if (c->slot_inflight[slot]) {
+        grouped[e] = 1;
+        wait_experts.push_back(e);
+        wait_slot.push_back(slot);
+      }
     } else {
       ++c->misses;
-      is_miss[e] = 1;
+      c->slot_prefetched[slot] = 0;
+      grouped[e] = 1;
       miss_experts.push_back(e);
+      miss_slot.push_back(slot);
     }
   }
   c->h_table[E] = c->has_shared ? c->d_shared + (size_t)layer * c->rec_bytes : nullptr;
 
+  // pass order: ready experts (and the shared expert) first, then each waiting expert's
+  // passes (read-ahead copies in flight, then misses)
+  std::vector<int> group_experts(wait_experts);
+  group_experts.insert(group_experts.end(), miss_experts.begin(), miss_experts.end());
+  int n_first = 0;
+  for (int p = 0; p < n_pass; ++p) {
+    const bool shared_pass = p >= n_routed;
+    if (shared_pass || !grouped[pexp[p]]) c->h_order[n_first++] = p;
+  }
+  std::vector<int> group_begin(group_experts.size() + 1);
+  int pos = n_first;
+  for (size_t m = 0; m < group_experts.size(); ++m) {
+    group_begin[m] = pos;
+    for (int p = 0; p < n_routed; ++p)
+      if (pexp[p] == group_experts[m]) c->h_order[pos++] = p;
+  }
+  group_begin[group_experts.size()] = pos;
+  // the record table and pass order go to the device before the miss copies are queued, so
+  // the ready experts' kernels do not wait behind the misses' transfers
+  CK(cudaMemcpyAsync(c->d_rec_table, c->h_table, (size_t)(E + 1) * sizeof(uint8_t*),
+                     cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(c->d_order, c->h_order, (size_t)n_pass * sizeof(int), cudaMemcpyHostToDevice, s));
+
   // miss copies on the side streams (round-robin), in ascending expert id, one event each
   const int ns = (int)std::min<size_t>(moe_ctx::kCopyStreams, std::max<size_t>(1, miss_experts.size()));
+  int bi = -1;
   if (!miss_experts.empty()) {
-    CK(cudaEventRecord(c->h2d_t0, c->side[0]));
-    for (int q = 1; q < ns; ++q) CK(cudaStreamWaitEvent(c->side[q], c->h2d_t0, 0));
+    moe_status bs = batch_begin(c, ns, &bi);
+    if (bs != MOE_OK) return bs;
   }
   for (size_t m = 0; m < miss_experts.size(); ++m) {
     cudaStream_t cs = c->side[m % ns];
-    const int e = miss_experts[m];
+    const int e = miss_experts[m], slot = miss_slot[m];
     const uint8_t* src = c->h_pool + ((size_t)layer * E + e) * c->rec_bytes;
+    // a read-ahead copy into the victim slot may still be running: this one goes after it
+    if (c->slot_inflight[slot]) CK(cudaStreamWaitEvent(cs, c->slot_ev[slot], 0));
+    c->slot_inflight[slot] = 0;
     cudaError_t ce;
     if (c->fail_copies > 0) {
       --c->fail_copies;
@@ -724,41 +958,16 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
       ce = cudaMemcpyAsync(c->h_table[e], src, c->rec_bytes, cudaMemcpyHostToDevice, cs);
     }
     if (ce != cudaSuccess) {
-      // the slot's content is unknown now: forget it
-      c->where.erase((long long)layer * E + e);
-      for (size_t i = 0; i < c->n_slots; ++i)
-        if (c->slot_key[i] == (long long)layer * E + e) {
-          c->slot_key[i] = -1;
-          if (c->slot_in_lru[i]) { c->lru.erase(c->lru_it[i]); c->slot_in_lru[i] = 0; }
-        }
+      forget_slot(c, slot);  // the slot's content is unknown now
       return cuda_fail(c);
     }
     CK(cudaEventRecord(c->copy_ev[m], cs));
     c->bytes_h2d += c->rec_bytes;
   }
-  if (!miss_experts.empty()) {
-    for (int q = 0; q < ns; ++q) CK(cudaEventRecord(c->h2d_t1[q], c->side[q]));
-    c->h2d_streams_used = ns;
-    c->h2d_pending = true;
+  if (bi >= 0) {
+    moe_status be = batch_end(c, bi);
+    if (be != MOE_OK) return be;
   }
-
-  // pass order: hits (and the shared expert) first, then each miss's passes
-  int n_first = 0;
-  for (int p = 0; p < n_pass; ++p) {
-    const bool shared_pass = p >= n_routed;
-    if (shared_pass || !is_miss[pexp[p]]) c->h_order[n_first++] = p;
-  }
-  std::vector<int> miss_begin(miss_experts.size() + 1);
-  int pos = n_first;
-  for (size_t m = 0; m < miss_experts.size(); ++m) {
-    miss_begin[m] = pos;
-    for (int p = 0; p < n_routed; ++p)
-      if (pexp[p] == miss_experts[m]) c->h_order[pos++] = p;
-  }
-  miss_begin[miss_experts.size()] = pos;
-  CK(cudaMemcpyAsync(c->d_rec_table, c->h_table, (size_t)(E + 1) * sizeof(uint8_t*),
-                     cudaMemcpyHostToDevice, s));
-  CK(cudaMemcpyAsync(c->d_order, c->h_order, (size_t)n_pass * sizeof(int), cudaMemcpyHostToDevice, s));
 
   ExpertArgs a = expert_args(c, c->d_rec_table, x, T);
   a.range.order = c->d_order;
@@ -767,14 +976,22 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     a.range.p_end = n_first;
     CK(launch_experts(c, a, s));
   }
-  for (size_t m = 0; m < miss_experts.size(); ++m) {
-    CK(cudaStreamWaitEvent(s, c->copy_ev[m], 0));
-    a.range.p_begin = miss_begin[m];
-    a.range.p_end = miss_begin[m + 1];
+  for (size_t m = 0; m < group_experts.size(); ++m) {
+    if (m < wait_experts.size()) {
+      const int slot = wait_slot[m];
+      CK(cudaStreamWaitEvent(s, c->slot_ev[slot], 0));
+      c->slot_inflight[slot] = 0;  // later copies into the slot follow a host sync past these kernels
+    } else {
+      CK(cudaStreamWaitEvent(s, c->copy_ev[m - wait_experts.size()], 0));
+    }
+    a.range.p_begin = group_begin[m];
+    a.range.p_end = group_begin[m + 1];
     CK(launch_experts(c, a, s));
   }
   CK(launch_combine(ca, s));
   c->last_T[layer] = T;
+  if (c->readahead && layer + 1 < c->cfg.num_layers && layer_ready(c, layer + 1) == MOE_OK)
+    return readahead(c, layer + 1, x, T);
   return MOE_OK;
 }
 
@@ -837,16 +1054,7 @@ moe_status moe_stats(moe_ctx* c, moe_stats_t* out) {
   moe_status st = check_device(c);
   DevCounters dc{};
   if (cudaMemcpy(&dc, c->d_counters, sizeof(dc), cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_fail(c);
-  if (c->h2d_pending && st == MOE_OK) {
-    float span = 0.f;
-    for (int q = 0; q < c->h2d_streams_used; ++q) {
-      float ms = 0.f;
-      if (cudaEventElapsedTime(&ms, c->h2d_t0, c->h2d_t1[q]) == cudaSuccess && ms > span) span = ms;
-      cudaGetLastError();
-    }
-    c->h2d_ms += span;
-    c->h2d_pending = false;
-  }
+  if (st == MOE_OK && c->streamed) batch_drain(c, true);
   memset(out, 0, sizeof(*out));
   out->forwards = dc.forwards;
   out->tokens = dc.tokens;
@@ -859,6 +1067,8 @@ moe_status moe_stats(moe_ctx* c, moe_stats_t* out) {
   out->record_bytes = c->rec_bytes;
   out->cache_slots = c->n_slots;
   out->h2d_ms = c->h2d_ms;
+  out->prefetches = c->prefetches;
+  out->prefetch_hits = c->prefetch_hits;
   return st;
 }
 
@@ -868,8 +1078,17 @@ moe_status moe_reset_stats(moe_ctx* c) {
   moe_status st = check_device(c);
   if (st != MOE_OK) return st;
   CK(cudaMemset(c->d_counters, 0, sizeof(DevCounters)));
+  if (c->streamed) batch_drain(c, true);
   c->hits = c->misses = c->bytes_h2d = 0;
+  c->prefetches = c->prefetch_hits = 0;
   c->h2d_ms = 0.0;
+  return MOE_OK;
+}
+
+moe_status moe_set_readahead(moe_ctx* c, int enable) {
+  if (!c || enable < 0 || enable > 1) return MOE_EINVAL;
+  if (!c->streamed) return enable ? MOE_EINVAL : MOE_OK;
+  c->readahead = enable;
   return MOE_OK;
 }
 

@@ -35,7 +35,8 @@ class Config(ctypes.Structure):
 class Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_ulonglong) for n in (
         "forwards", "tokens", "lookups", "hits", "misses", "bytes_expert_touched",
-        "bytes_router", "bytes_h2d", "record_bytes", "cache_slots")] + [("h2d_ms", ctypes.c_double)]
+        "bytes_router", "bytes_h2d", "record_bytes", "cache_slots")] + [("h2d_ms", ctypes.c_double)] + [
+        (n, ctypes.c_ulonglong) for n in ("prefetches", "prefetch_hits")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -71,11 +72,13 @@ def lib():
     L.moe_profile.argtypes = [vp, i]
     L.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i)]
     L.moe_debug_fail_copies.argtypes = [vp, i]
+    L.moe_set_readahead.argtypes = [vp, i]
     L.moe_debug_wait_timeout.argtypes = [vp, u64, vp, ctypes.POINTER(i)]
     for name in ("moe_create", "moe_register_router", "moe_register_expert", "moe_forward",
                  "moe_get_routing", "moe_residual_rmsnorm", "moe_stats", "moe_reset_stats",
                  "moe_destroy", "moe_debug_fail_copies", "moe_debug_wait_timeout",
-                 "moe_profile", "moe_profile_read", "moe_forward_residual", "moe_route_noalloc"):
+                 "moe_profile", "moe_profile_read", "moe_forward_residual", "moe_route_noalloc",
+                 "moe_set_readahead"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -212,6 +215,10 @@ class Context:
         self._check(lib().moe_reset_stats(self._h), "moe_reset_stats")
 
     # -- measurement
+    def set_readahead(self, enable=True):
+        """Streamed contexts: predict the next layer's experts and start their copies early."""
+        self._check(lib().moe_set_readahead(self._h, 1 if enable else 0), "moe_set_readahead")
+
     def profile(self, enable=True):
         self._check(lib().moe_profile(self._h, 1 if enable else 0), "moe_profile")
 

@@ -188,3 +188,71 @@ def test_fused_stack_step_equals_separate_calls(spec):
         outs.append(x.cpu().numpy().copy())
     ctx.close()
     np.testing.assert_array_equal(np.stack(outs), ref)
+
+
+def _fused_run(ctx, spec, xbits_seq):
+    import torch
+    T, H = xbits_seq.shape[1], spec.H
+    outs = []
+    x = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    y = torch.zeros_like(x)
+    xn = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    for xb in xbits_seq:
+        x.copy_(torch.from_numpy(S.bf16_bits_to_f32(xb)))
+        for l in range(spec.layers):
+            ctx.forward_residual(l, x, None if l == 0 else y, xn, y, T)
+        ctx.residual_rmsnorm(x, y, xn)
+        torch.cuda.synchronize()
+        outs.append(x.cpu().numpy().copy())
+    return np.stack(outs)
+
+
+@pytest.mark.parametrize("spec", [SPEC, SPEC4])
+def test_readahead_changes_timing_not_bits(spec):
+    """Read-ahead copies of predicted experts (right or wrong) leave every bit as the
+    resident run's, including when a miss or another prediction evicts a slot whose
+    read-ahead copy is still in flight (the smallest cache)."""
+    seq = _tokens(spec, 12)
+    ref_ctx = make_context(spec, 1)
+    ref, ref_routes = _stack_run(ref_ctx, spec, seq)
+    ref_f = _fused_run(ref_ctx, spec, seq)
+    ref_ctx.close()
+    probe = make_context(spec, 1, hbm_cache_bytes=1 << 40, register=False)
+    rb = probe.stats()["record_bytes"]
+    probe.close()
+    for slots in (2 * spec.k, 3 * spec.k, 4 * spec.k):
+        ctx = make_context(spec, 1, hbm_cache_bytes=slots * rb)
+        ctx.set_readahead(True)
+        out, routes = _stack_run(ctx, spec, seq)
+        out_f = _fused_run(ctx, spec, seq)
+        st = ctx.stats()
+        ctx.close()
+        assert all(np.array_equal(a, b) for a, b in zip(routes, ref_routes))
+        np.testing.assert_array_equal(out, ref)
+        np.testing.assert_array_equal(out_f, ref_f)
+        assert st["prefetches"] > 0
+        assert 0 <= st["prefetch_hits"] <= st["prefetches"]
+        assert st["hits"] + st["misses"] == st["lookups"]
+        assert st["bytes_h2d"] == (st["misses"] + st["prefetches"]) * rb
+        assert st["h2d_ms"] > 0
+
+
+def test_readahead_arguments():
+    import routed_expert_ffn_03_gb300 as M
+    from routed_expert_ffn_03_gb300.moe import lib
+    res = make_context(SPEC, 1, register=False)
+    with pytest.raises(M.MoeError) as ei:       # nothing to read ahead into: all resident
+        res.set_readahead(True)
+    assert ei.value.status == M.EINVAL
+    res.set_readahead(False)
+    res.close()
+    probe = make_context(SPEC, 1, hbm_cache_bytes=1 << 40, register=False)
+    rb = probe.stats()["record_bytes"]
+    probe.close()
+    ctx = make_context(SPEC, 1, hbm_cache_bytes=2 * SPEC.k * rb, register=False)
+    assert lib().moe_set_readahead(ctx._h, 2) == M.EINVAL
+    assert lib().moe_set_readahead(ctx._h, -1) == M.EINVAL
+    assert lib().moe_set_readahead(None, 1) == M.EINVAL
+    ctx.set_readahead(True)
+    ctx.set_readahead(False)
+    ctx.close()

@@ -270,6 +270,58 @@ def cpu_baseline(cfg, device):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def lru_hit_rate(trace, slots, k_use):
+    """Hit rate of a record-granular LRU of `slots` records over a routing trace, cold
+    start, lookups of each (token, layer) in ascending expert id, the current layer's
+    experts pinned (the engine's rules).  trace: list over (token, layer) of the routed ids
+    in rank order; only the first k_use of each are looked up."""
+    from collections import OrderedDict
+    lru = OrderedDict()
+    hits = looks = 0
+    for layer, ids in trace:
+        cur = sorted(set(int(e) for e in ids[:k_use]))
+        pinned = set()
+        for e in cur:
+            key = (layer, e)
+            looks += 1
+            if key in lru:
+                hits += 1
+                lru.move_to_end(key)
+            else:
+                if len(lru) >= slots:
+                    for victim in lru:          # least recent first
+                        if victim[0] != layer or victim[1] not in pinned:
+                            break
+                    del lru[victim]
+                lru[key] = True
+            pinned.add(e)
+    return hits / max(1, looks)
+
+
+def hit_sweep(ctx, cfg, layers_fn, x, x0_dev, n_tokens, stream):
+    """Routing trace of n_tokens through the stack (results do not depend on the cache), then
+    the LRU hit rate at several cache budgets for top-k and top-k/2 (the first half of each
+    top-k list is the top-(k/2) selection)."""
+    import torch
+    trace = []
+    with torch.cuda.stream(stream):
+        for i in range(n_tokens):
+            x.copy_(x0_dev[i % x0_dev.shape[0]])
+            for l in range(cfg["layers"]):
+                layers_fn(l)
+                idx, _ = ctx.get_routing(l)
+                trace.append((l, idx[0]))
+    rec = ctx.stats()["record_bytes"]
+    rows = []
+    for gb in (8, 16, 32, 64, 96, 128):
+        slots = int(gb * 1e9 // rec)
+        rows.append({"budget_gb": gb, "slots": slots,
+                     "hit_rate_k%d" % cfg["k"]: round(lru_hit_rate(trace, slots, cfg["k"]), 4),
+                     "hit_rate_k%d" % (cfg["k"] // 2): round(lru_hit_rate(trace, slots, cfg["k"] // 2), 4)})
+    return {"tokens": n_tokens, "method": "routing trace of the stack (T=1, domain-local inputs) replayed through "
+            "the engine's LRU rules on the host, cold start", "rows": rows}
+
+
 def run_gpu(args, cfg, rank, world, device):
     import torch
     torch.cuda.set_device(device)
@@ -429,6 +481,12 @@ def run_gpu(args, cfg, rank, world, device):
         link = measure_link_gbs(device)
         miss_gbs = st["bytes_h2d"] / max(1e-9, st["h2d_ms"] / 1e3) / 1e9 if st["h2d_ms"] else None
         out["hit_series_per64"] = hit_series
+        if args.hit_sweep and T == 1:
+            ctx.set_readahead(False)
+
+            def one_layer(l):
+                ctx.forward_residual(l, x, None if l == 0 else y, xn, y, T)
+            out["hit_rate_vs_cache"] = hit_sweep(ctx, cfg, one_layer, x, x0_dev, args.hit_sweep, stream)
         out["streaming"] = {
             "readahead": bool(args.readahead),
             "misses_per_token": round(st["misses"] / max(1, K), 2), "hits": st["hits"], "misses": st["misses"],
@@ -530,6 +588,9 @@ def main():
     ap.add_argument("--prof-steps", type=int, default=16, help="replays of the per-kernel event graph")
     ap.add_argument("--readahead", type=int, default=1, choices=[0, 1],
                     help="streamed configs: predict the next layer's experts and copy them early")
+    ap.add_argument("--hit-sweep", type=int, default=0, metavar="TOKENS",
+                    help="streamed configs: after the timed run, the LRU hit rate vs cache budget over a "
+                         "routing trace of this many tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

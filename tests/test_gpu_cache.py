@@ -256,3 +256,26 @@ def test_readahead_arguments():
     ctx.set_readahead(True)
     ctx.set_readahead(False)
     ctx.close()
+
+
+def test_engine_lru_matches_the_host_replay():
+    """The cache's hits and misses equal a host replay of the same routing trace through
+    the LRU rules the hit-rate sweep uses (record granularity, ascending ids, current layer
+    kept)."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    probe = make_context(SPEC, 1, hbm_cache_bytes=1 << 40, register=False)
+    rb = probe.stats()["record_bytes"]
+    probe.close()
+    seq = _tokens(SPEC, 16)
+    for slots in (2 * SPEC.k, 3 * SPEC.k + 1):
+        ctx = make_context(SPEC, 1, hbm_cache_bytes=slots * rb)
+        _, routes = _stack_run(ctx, SPEC, seq)
+        st = ctx.stats()
+        ctx.close()
+        trace = [(i % SPEC.layers, r[0]) for i, r in enumerate(routes)]
+        rate = bench.lru_hit_rate(trace, slots, SPEC.k)
+        assert st["lookups"] == sum(len(set(r[0])) for r in routes)
+        assert st["hits"] == round(rate * st["lookups"])

@@ -144,7 +144,7 @@ moe_status moe_register_expert(moe_ctx* ctx, int layer, int expert, const void* 
 size_t moe_expert_blob_bytes(int wfmt, int hidden, int ffn);
 
 /* One MoE layer on T tokens: out[T,H] (fp32) = combine of the routed experts (+ shared)
- * applied to x[T,H] (bf16 bits, row-major).  x and out are device pointers, x 8-byte
+ * applied to x[T,H] (bf16 bits, row-major).  x and out are device pointers, x 16-byte
  * aligned.
  * Resident mode: fully stream-ordered, never blocks the host, capturable in a CUDA
  * graph.  Streamed mode: blocks the host once per call to read the routing back, then
@@ -156,8 +156,8 @@ moe_status moe_forward(moe_ctx* ctx, int layer, const void* x_bf16, float* out, 
 /* One layer of the residual stack, fused:  if y_prev != NULL: x += y_prev;
  * xn = bf16(x / sqrt(mean(x^2) + eps));  y = layer(xn)  (as moe_forward).
  * x fp32 [T,H] in/out, y_prev fp32 [T,H] or NULL (it may be the same buffer as y),
- * xn bf16 bits [T,H] out, y fp32 [T,H] out; all device pointers, x and y_prev 16-byte
- * aligned, xn 8-byte aligned (MOE_EINVAL otherwise).  Same bits as
+ * xn bf16 bits [T,H] out, y fp32 [T,H] out; all device pointers, x, y_prev and xn 16-byte
+ * aligned (MOE_EINVAL otherwise).  Same bits as
  * moe_residual_rmsnorm followed by moe_forward; for small T the norm runs inside the
  * router kernel instead of a kernel of its own. */
 moe_status moe_forward_residual(moe_ctx* ctx, int layer, float* x, const float* y_prev, uint16_t* xn,

@@ -830,6 +830,11 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
 
   if (!c->streamed) {
     ExpertArgs a = expert_args(c, c->d_rec_table + (size_t)layer * (E + 1), x, T);
+    a.slab_layer = c->d_slab + (size_t)layer * c->E1 * c->rec_bytes;
+    a.rec_bytes = c->rec_bytes;
+    // one token: exactly one pass per selected expert (+ the shared one), known here, so
+    // the expert kernels need not read the count from the plan
+    if (T == 1 && c->big_min == 0) a.range.p_end = k + c->has_shared;
     cudaEvent_t* ev = c->prof ? &c->prof_ev[(size_t)layer * 5] : nullptr;
     if (ev) CK(cudaEventRecordWithFlags(ev[1], s, cudaEventRecordExternal));
     if (c->cfg.wfmt == MOE_W_INT4_G128) {
@@ -997,7 +1002,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
 
 moe_status moe_forward(moe_ctx* c, int layer, const void* x, float* out, int T, void* stream) {
   if (!c || !x || !out || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
-  if ((uintptr_t)x & 7) return MOE_EINVAL;
+  if ((uintptr_t)x & 15) return MOE_EINVAL;
   if (T < 1 || T > c->cfg.max_tokens) return MOE_EINVAL;
   if (c->sticky != MOE_OK) return c->sticky;
   moe_status rs = layer_ready(c, layer);
@@ -1010,7 +1015,7 @@ moe_status moe_forward_residual(moe_ctx* c, int layer, float* x, const float* y_
                                 int T, float eps, void* stream) {
   if (!c || !x || !xn || !y || layer < 0 || layer >= c->cfg.num_layers) return MOE_EINVAL;
   if (T < 1 || T > c->cfg.max_tokens) return MOE_EINVAL;
-  if (((uintptr_t)x & 15) || ((uintptr_t)y_prev & 15) || ((uintptr_t)xn & 7)) return MOE_EINVAL;
+  if (((uintptr_t)x & 15) || ((uintptr_t)y_prev & 15) || ((uintptr_t)xn & 15)) return MOE_EINVAL;
   if (c->sticky != MOE_OK) return c->sticky;
   moe_status rs = layer_ready(c, layer);
   if (rs != MOE_OK) return rs;

@@ -172,14 +172,47 @@ __device__ __forceinline__ void build_bfrags(uint2* xf, int nks16, int nb, int t
   }
 }
 
+// The 8 fragment words of k-step kk of token slot ts (4 pairs x hi/lo) from its 16 bf16
+// inputs (u0, u1: inputs 2i, 2i+1 in word i), into xf[column n*4 + p][k-step].
+__device__ __forceinline__ void bfrag_kstep(uint2* xf, int kstride, int ts, int kk, const uint4& u0, const uint4& u1) {
+  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp) {
+    float f[10];
+    f[0] = __uint_as_float(w[pp] << 16);
+    f[1] = __uint_as_float(w[pp] & 0xffff0000u);
+    f[8] = __uint_as_float(w[pp + 4] << 16);
+    f[9] = __uint_as_float(w[pp + 4] & 0xffff0000u);
+    xf[((2 * ts) * 4 + pp) * kstride + kk] = bfrag(f, 0);
+    xf[((2 * ts + 1) * 4 + pp) * kstride + kk] = bfrag(f, 1);
+  }
+}
+
+// B fragments of all K for the tokens tok[0..ntok) of a pass straight from the bf16 input:
+// one thread per (token, k-step) reads its 16 inputs with two 16-byte loads.
+__device__ __forceinline__ void build_bfrags_x(uint2* xf, const uint16_t* x, int H, const int (&tok)[I4_PMAX],
+                                               int ntok, int tid, int nthr) {
+  const int nks16 = H / 16, ks = i4_kstride(nks16);
+  for (int e = tid; e < ntok * nks16; e += nthr) {
+    const int ts = e / nks16, kk = e - ts * nks16;
+    int t = tok[0];
+#pragma unroll
+    for (int q = 1; q < I4_PMAX; ++q)
+      if (ts == q) t = tok[q];
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + kk * 16);
+    bfrag_kstep(xf, ks, ts, kk, __ldg(src), __ldg(src + 1));
+  }
+}
+
 // ------------------------------------------------------------------ warp-local staging
 // Every warp streams its own tasks: lane 0 starts the bulk copy of task j + D into the
 // ring slot task j has just released, so the block's warps issue copies in parallel and
 // each keeps D tasks in flight.  full[w][d] completes when slot d of warp w has landed.
+// No proxy fence is needed before the copy: the warp's shared-memory reads of the slot
+// returned their data into registers that the task's mma instructions consumed, which
+// the warp issued before this point, so the copy cannot overwrite data still being read.
 __device__ __forceinline__ void stage_issue(int lane, uint32_t full, uint32_t dst, const void* src, uint32_t bytes) {
   if (lane == 0) {
-    // the slot's previous contents were read through the generic proxy
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive_expect_tx(full, bytes);
     bulk_g2s(dst, src, bytes, full);
   }
@@ -212,7 +245,7 @@ __device__ __forceinline__ void stage_drain(uint32_t full0, int issued, int cons
 __device__ __forceinline__ void load_recs(const uint8_t** recs, const ExpertArgs& a, int p_begin, int pi0, int pi1,
                                           int tid, int nthr) {
   for (int q = tid; q < pi1 - pi0; q += nthr)
-    recs[q] = a.rec_table[__ldcg(a.plan.pass_expert + pass_of(a, p_begin, pi0 + q))];
+    recs[q] = expert_record(a, __ldcg(a.plan.pass_expert + pass_of(a, p_begin, pi0 + q)));
 }
 
 // ------------------------------------------------------------------ gate/up
@@ -248,6 +281,15 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
     for (int i = 0; i < NW * D; ++i) mbar_init(smem_u32(bars + i), 1);
     s_abort = 0;
     mbar_fence_init();
+  }
+  // one token: every pass multiplies the same x, so its fragments are built once, from
+  // loads issued before this block's weight stream starts (they would queue behind it)
+  const bool one = a.T == 1 && a.H / 16 <= nthr;
+  uint4 xu0 = make_uint4(0u, 0u, 0u, 0u), xu1 = xu0;
+  if (one && t0 < t1 && (int)threadIdx.x < a.H / 16) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + threadIdx.x * 16);
+    xu0 = __ldg(src);
+    xu1 = __ldg(src + 1);
   }
   load_recs(s_rec, a, p_begin, pi0, pi1, threadIdx.x, nthr);
   __syncthreads();
@@ -286,20 +328,21 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
     const int pi = seg / per_pass;
     const int seg_end = min(t1, (pi + 1) * per_pass);
     const int pass = pass_of(a, p_begin, pi);
-    const int ntok = __ldcg(a.plan.pass_ntok + pass);
+    // one token per forward: the pass has that token alone, no plan read needed
+    const int ntok = a.T == 1 ? 1 : __ldcg(a.plan.pass_ntok + pass);
     const int nb = 2 * ntok;
     int tok[I4_PMAX];
 #pragma unroll
-    for (int q = 0; q < I4_PMAX; ++q) tok[q] = q < ntok ? __ldcg(a.plan.pass_tok + pass * I4_PMAX + q) : 0;
-    named_sync(1, nthr);
-    build_bfrags(xfrag, a.H / 16, nb, threadIdx.x, nthr, [&](int ts, int k) {
-      int t = tok[0];
-#pragma unroll
-      for (int q = 1; q < I4_PMAX; ++q)
-        if (ts == q) t = tok[q];
-      return bf16_bits_to_float(a.x[(size_t)t * a.H + k]);
-    });
-    named_sync(1, nthr);
+    for (int q = 0; q < I4_PMAX; ++q) tok[q] = (q < ntok && a.T > 1) ? __ldcg(a.plan.pass_tok + pass * I4_PMAX + q) : 0;
+    if (!(one && seg > t0)) {
+      named_sync(1, nthr);
+      if (one) {
+        if ((int)threadIdx.x < a.H / 16) bfrag_kstep(xfrag, i4_kstride(a.H / 16), 0, threadIdx.x, xu0, xu1);
+      } else {
+        build_bfrags_x(xfrag, a.x, a.H, tok, ntok, threadIdx.x, nthr);
+      }
+      named_sync(1, nthr);
+    }
     float* part = a.part_gu + (size_t)pass * 2 * nks * I4_PMAX * rows32;
     const uint2* xcol = xfrag + i4_lane_col(lane, nb) * i4_kstride(a.H / 16);
     int local = ti - pi * per_pass;          // compute cursor within the pass
@@ -404,7 +447,9 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
       }
     }
   };
-  while (j_issue < min(D, nw)) issue_next();
+  // one task per warp streams before the wait; the rest of the ring fills after this
+  // block's gate/up partials have been read (those reads would queue behind a full ring)
+  if (j_issue < min(1, nw)) issue_next();
 
   pdl_wait();  // the gate/up partials come from the kernel before
   pdl_launch_dependents();
@@ -419,7 +464,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
     const int seg_end = min(t1, (u + 1) * ntask);
     const int pi = u / nks, ks = u - pi * nks;
     const int pass = pass_of(a, p_begin, pi);
-    const int ntok = __ldcg(a.plan.pass_ntok + pass);
+    const int ntok = a.T == 1 ? 1 : __ldcg(a.plan.pass_ntok + pass);
     const int nb = 2 * ntok;
     const int ng = min(I4_KS, NG - ks * I4_KS);
     const int kbase = ks * I4_KS * I4_GROUP, kvalid = ng * I4_GROUP;
@@ -457,6 +502,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
     build_bfrags(xfrag, I4_SLICE_KSTEPS, nb, threadIdx.x, nthr,
                  [&](int ts, int k) { return vin[ts * (I4_KS * I4_GROUP) + k]; });
     named_sync(1, nthr);
+    while (j_issue < min(D, nw)) issue_next();
     float* dst0 = a.part_d + ((size_t)pass * nks + ks) * I4_PMAX * rows32;
     const uint2* xcol = xfrag + i4_lane_col(lane, nb) * i4_kstride(I4_SLICE_KSTEPS);
     for (; ti < seg_end; ti += NW) {

@@ -53,6 +53,8 @@ struct PassRange {
 
 struct ExpertArgs {
   const uint8_t* const* rec_table;  // [E + 1] record pointers (E = shared expert)
+  const uint8_t* slab_layer;        // resident: this layer's records, expert e at e * rec_bytes
+  size_t rec_bytes;                 //   (null when streamed: records are found through rec_table)
   PlanPtrs plan;
   int H, F, E, T, max_tokens;
   const uint16_t* x;                // bf16 [T][H] (gate/up input)
@@ -63,6 +65,14 @@ struct ExpertArgs {
   uint32_t* status;
   unsigned long long budget;
 };
+#ifdef __CUDACC__
+// Record of expert e (E = the shared expert): resident records sit at a fixed stride, so
+// no table read is needed; streamed records are wherever the cache put them.
+__device__ __forceinline__ const uint8_t* expert_record(const ExpertArgs& a, int e) {
+  return a.slab_layer ? a.slab_layer + (size_t)e * a.rec_bytes : a.rec_table[e];
+}
+#endif
+
 cudaError_t int4_set_attributes(int H, int max_tokens);
 cudaError_t rvq_set_attributes();
 cudaError_t launch_int4_gateup(const ExpertArgs& a, int grid, cudaStream_t s);

@@ -105,7 +105,7 @@ __device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, i
   const int pi = pm / mats;
   U.pass = a.range.order ? __ldcg(a.range.order + p_begin + pi) : p_begin + pi;
   U.expert = __ldcg(a.plan.pass_expert + U.pass);
-  U.base = a.rec_table[U.expert] + (DOWN ? rg.off[2] : (U.m == 0 ? rg.off[0] : rg.off[1]));
+  U.base = expert_record(a, U.expert) + (DOWN ? rg.off[2] : (U.m == 0 ? rg.off[0] : rg.off[1]));
   return U;
 }
 

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
     const int pass0 = __ldcg(a.plan.big + 3 * I.grp + 1);
     const int ntok = __ldcg(a.plan.big + 3 * I.grp + 2);
     const int N = max(16, (2 * ntok + 15) & ~15);
-    const uint8_t* mat = a.rec_table[expert] + (DOWN ? rg.off[2] : (I.m == 0 ? rg.off[0] : rg.off[1]));
+    const uint8_t* mat = expert_record(a, expert) + (DOWN ? rg.off[2] : (I.m == 0 ? rg.off[0] : rg.off[1]));
     const int rb0 = I.tile * 4, nrb = min(4, g.ntask - rb0);
 
     // codebooks and codes of this tile and slice

@@ -118,6 +118,157 @@ __device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src
   }
 }
 
+// Phase 2 of the router, in one block: top-k per token from the logits lsrc [T][E]
+// (global memory when global_src), the weights, and the bucketing of the (token, rank)
+// pairs into passes.  s_cnt must be zero and the logits complete (after a barrier).
+__device__ __forceinline__ void router_finish(const RouterArgs& a, const float* lsrc, bool global_src, int* s_cnt,
+                                              int* s_off, int* s_idx, int* s_pos, int* s_routed) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int E = a.E, T = a.T, k = a.k, pmax = a.pmax;
+  // ---------------- phase 2a: top-k per token (one warp per token)
+  for (int t = warp; t < T; t += nwarps) {
+    const float* src = lsrc + (size_t)t * E;
+    if (E <= 128) topk_token<4>(a, src, global_src, t, lane, s_idx);
+    else if (E <= 256) topk_token<8>(a, src, global_src, t, lane, s_idx);
+    else if (E <= 512) topk_token<16>(a, src, global_src, t, lane, s_idx);
+    else topk_token<32>(a, src, global_src, t, lane, s_idx);
+  }
+  __syncthreads();
+
+  // ---------------- phase 2b: position of each pair within its expert (tokens ascending)
+  if (warp == 0) {
+    for (int t = 0; t < T; ++t) {
+      if (lane < k) {
+        const int ee = s_idx[t * k + lane];   // the k experts of a token are distinct
+        const int pos = s_cnt[ee];
+        s_cnt[ee] = pos + 1;
+        s_pos[t * k + lane] = pos;
+      }
+      __syncwarp();
+    }
+    // exclusive scan over experts of (passes, unique flag); lane owns a contiguous run
+    const int run = cdiv(E, 32);
+    const int e0 = min(E, lane * run), e1 = min(E, e0 + run);
+    int np = 0, nu = 0;
+    for (int ee = e0; ee < e1; ++ee) {
+      np += cdiv(s_cnt[ee], pmax);
+      nu += s_cnt[ee] > 0;
+    }
+    int inp = np, inu = nu;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a1 = __shfl_up_sync(0xffffffffu, inp, o);
+      const int a2 = __shfl_up_sync(0xffffffffu, inu, o);
+      if (lane >= o) { inp += a1; inu += a2; }
+    }
+    int off = inp - np, uoff = inu - nu;
+    for (int ee = e0; ee < e1; ++ee) {
+      s_off[ee] = off;
+      const int c = s_cnt[ee];
+      if (c > 0) a.plan.uniq[uoff++] = ee;
+      off += cdiv(c, pmax);
+    }
+    const int tot_p = __shfl_sync(0xffffffffu, inp, 31);
+    const int tot_u = __shfl_sync(0xffffffffu, inu, 31);
+    if (lane == 0) {
+      const int nsh = a.has_shared ? cdiv(T, pmax) : 0;
+      a.plan.hdr->n_pass = tot_p + nsh;
+      a.plan.hdr->n_routed_pass = tot_p;
+      a.plan.hdr->n_uniq = tot_u;
+      a.plan.hdr->T = T;
+      *s_routed = tot_p;
+      DevCounters* dc = a.counters;
+      atomicAdd(&dc->forwards, 1ull);
+      atomicAdd(&dc->tokens, (unsigned long long)T);
+      atomicAdd(&dc->lookups, (unsigned long long)tot_u);
+      atomicAdd(&dc->bytes_touched, (unsigned long long)(tot_u + (a.has_shared ? 1 : 0)) * a.record_bytes);
+      atomicAdd(&dc->bytes_router, (unsigned long long)E * a.H * 4ull);
+    }
+  }
+  __syncthreads();
+
+  // ---------------- phase 2c: pass tables
+  const int routed_passes = *s_routed;
+  for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
+    const int c = s_cnt[ee];
+    for (int i = 0; i * pmax < c; ++i) {
+      a.plan.pass_expert[s_off[ee] + i] = ee;
+      a.plan.pass_ntok[s_off[ee] + i] = min(pmax, c - i * pmax);
+    }
+  }
+  for (int q = threadIdx.x; q < T * k; q += blockDim.x) {
+    const int ee = s_idx[q], pos = s_pos[q];
+    const int pass = s_off[ee] + pos / pmax, slot = pos % pmax;
+    a.plan.pass_tok[pass * pmax + slot] = q / k;
+    a.plan.pair_pass[q] = pass;
+    a.plan.pair_slot[q] = slot;
+  }
+  if (a.has_shared) {
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+      const int pass = routed_passes + t / pmax, slot = t % pmax;
+      a.plan.pass_tok[pass * pmax + slot] = t;
+      a.plan.shared_pass[t] = pass;
+      a.plan.shared_slot[t] = slot;
+      if (slot == 0) {
+        a.plan.pass_expert[pass] = E;
+        a.plan.pass_ntok[pass] = min(pmax, T - t);
+      }
+    }
+  }
+  // dense groups (pmax == 1: one pass per token): experts with >= big_min tokens go to the
+  // tcgen05 path in balanced chunks of <= GEMM_MAX_TOKENS, every other pass to the
+  // per-token path, both lists in ascending expert id (the shared expert last) then token
+  // order.  Warp 0: lane owns a contiguous run of experts, an exclusive scan places it.
+  if (warp == 0) {
+    if (a.big_min > 0) {
+      const int E1 = E + (a.has_shared ? 1 : 0);
+      const int run = cdiv(E1, 32);
+      const int e0 = min(E1, lane * run), e1 = min(E1, e0 + run);
+      auto cnt_of = [&](int ee) { return ee < E ? s_cnt[ee] : T; };
+      auto first_of = [&](int ee) { return ee < E ? s_off[ee] : routed_passes; };
+      int nb = 0, ns = 0;
+      for (int ee = e0; ee < e1; ++ee) {
+        const int c = cnt_of(ee), nc = big_chunks(c, a.big_min);
+        nb += nc;
+        ns += nc ? 0 : c;
+      }
+      int ib = nb, is = ns;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a1 = __shfl_up_sync(0xffffffffu, ib, o);
+        const int a2 = __shfl_up_sync(0xffffffffu, is, o);
+        if (lane >= o) { ib += a1; is += a2; }
+      }
+      int ob = ib - nb, os = is - ns;
+      for (int ee = e0; ee < e1; ++ee) {
+        const int c = cnt_of(ee), first = first_of(ee), nc = big_chunks(c, a.big_min);
+        if (nc) {
+          const int base = c / nc, rem = c % nc;
+          int start = 0;
+          for (int q = 0; q < nc; ++q) {
+            const int sz = base + (q < rem ? 1 : 0);
+            a.plan.big[3 * ob + 0] = ee;
+            a.plan.big[3 * ob + 1] = first + start;
+            a.plan.big[3 * ob + 2] = sz;
+            ++ob;
+            start += sz;
+          }
+        } else {
+          for (int i = 0; i < c; ++i) a.plan.small_order[os++] = first + i;
+        }
+      }
+      if (lane == 31) {
+        a.plan.hdr->n_big = ib;
+        a.plan.hdr->n_small = is;
+      }
+    } else if (lane == 0) {
+      a.plan.hdr->n_big = 0;
+      a.plan.hdr->n_small = routed_passes + (a.has_shared ? cdiv(T, pmax) : 0);
+    }
+    if (lane == 0) *a.ticket = 0u;  // ready for the next launch (stream-ordered)
+  }
+}
+
 // MINB = blocks per SM the registers must allow: 3 where the grid is larger than two
 // blocks per SM (so it still runs in one wave), else 1 (no register cap).
 template <int MINB>
@@ -127,7 +278,6 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
   __shared__ float s_red[32];
   __shared__ int s_flag, s_routed;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
   const int NS = cdiv(a.H, RSW), NG = cdiv(a.E, REPB);
   const int sl = blockIdx.x % NS, g = blockIdx.x / NS;
   const int h0 = sl * RSW;
@@ -255,7 +405,7 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
   if (!s_flag) return;
   __threadfence();
 
-  const int E = a.E, T = a.T, k = a.k, pmax = a.pmax;
+  const int E = a.E, T = a.T, k = a.k;
   int* s_cnt = sm;                  // [E]
   int* s_off = s_cnt + E;           // [E]
   int* s_idx = s_off + E;           // [T*k]
@@ -286,152 +436,120 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
   }
   __syncthreads();
 
-  // ---------------- phase 2a: top-k per token (one warp per token)
-  for (int t = warp; t < T; t += nwarps) {
-    const float* src = two_level ? logits + (size_t)t * E : slog + t * E;
-    if (E <= 128) topk_token<4>(a, src, two_level, t, lane, s_idx);
-    else if (E <= 256) topk_token<8>(a, src, two_level, t, lane, s_idx);
-    else if (E <= 512) topk_token<16>(a, src, two_level, t, lane, s_idx);
-    else topk_token<32>(a, src, two_level, t, lane, s_idx);
-  }
-  __syncthreads();
+  router_finish(a, two_level ? logits : slog, two_level, s_cnt, s_off, s_idx, s_pos, &s_routed);
+}
 
-  // ---------------- phase 2b: position of each pair within its expert (tokens ascending)
-  if (warp == 0) {
+
+// ---------------------------------------------------------------- small problems, one block
+// When every (expert, slice) item fits one warp of a single 1024-thread block and the
+// bf16 input fits shared memory, one block does the whole router: no partials in global
+// memory, no fences, no tickets.  Warp w owns expert w / NS on slice w % NS and loads its
+// W slice before the wait; logits are the slices added in ascending order, as in
+// router_kernel, so both give the same bits.
+constexpr int RSMALL_THREADS = 1024;
+__host__ __device__ __forceinline__ bool router_small_fits(int H, int T, int E) {
+  return E * cdiv(H, RSW) <= RSMALL_THREADS / 32 && T * H <= 32768 && T <= 32;
+}
+size_t router_small_smem(int H, int T, int E, int k) {
+  return (size_t)T * H * 2 + (size_t)T * E * cdiv(H, RSW) * 4 + (size_t)T * E * 4 +
+         (size_t)(2 * E + 2 * T * k) * sizeof(int);
+}
+
+__global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) int sm[];
+  __shared__ float s_inv[ROUTER_FUSED_MAXT];
+  __shared__ float s_red[32];
+  __shared__ int s_routed;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.H, T = a.T, E = a.E, k = a.k;
+  const int NS = cdiv(H, RSW), items = E * NS;
+  const int e = warp / NS, sl = warp - e * NS, h0 = sl * RSW;
+  const bool live = warp < items;
+  const bool fused = a.xres != nullptr;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);                        // [T][H] bf16
+  float* spart = reinterpret_cast<float*>(xs + (size_t)T * H);           // [T][E][NS]
+  float* slog = spart + (size_t)T * E * NS;                              // [T][E]
+  int* s_cnt = reinterpret_cast<int*>(slog + (size_t)T * E);            // [E]
+  int* s_off = s_cnt + E;                                                // [E]
+  int* s_idx = s_off + E;                                                // [T*k]
+  int* s_pos = s_idx + T * k;                                            // [T*k]
+
+  float4 wv[RSW / 128];
+  {
+    const float* wr = a.W + (size_t)(live ? e : 0) * H;
+#pragma unroll
+    for (int i = 0; i < RSW / 128; ++i) {
+      const int h = h0 + 4 * (lane + 32 * i);
+      wv[i] = (live && h < H) ? __ldg(reinterpret_cast<const float4*>(wr + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  pdl_wait();  // x (and the residual) come from the kernels before
+  pdl_launch_dependents();
+  if (fused) {
     for (int t = 0; t < T; ++t) {
-      if (lane < k) {
-        const int ee = s_idx[t * k + lane];   // the k experts of a token are distinct
-        const int pos = s_cnt[ee];
-        s_cnt[ee] = pos + 1;
-        s_pos[t * k + lane] = pos;
+      const float inv = block_inv_rms(a.xres + (size_t)t * H, a.yprev ? a.yprev + (size_t)t * H : nullptr, H,
+                                      a.eps, s_red);
+      if (threadIdx.x == 0) s_inv[t] = inv;
+    }
+    __syncthreads();
+  }
+  for (int q = threadIdx.x; q < T * (H / 4); q += blockDim.x) {
+    const int t = q / (H / 4), h = 4 * (q - t * (H / 4));
+    const size_t o = (size_t)t * H + h;
+    uint2 v;
+    if (fused) {
+      float4 x4 = __ldcg(reinterpret_cast<const float4*>(a.xres + o));
+      if (a.yprev) {
+        const float4 y4 = __ldcg(reinterpret_cast<const float4*>(a.yprev + o));
+        x4.x += y4.x; x4.y += y4.y; x4.z += y4.z; x4.w += y4.w;
       }
-      __syncwarp();
+      const float inv = s_inv[t];
+      v.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.x * inv)) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.y * inv)) << 16);
+      v.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.z * inv)) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.w * inv)) << 16);
+      *reinterpret_cast<uint2*>(a.xn_out + o) = v;
+    } else {
+      v = __ldg(reinterpret_cast<const uint2*>(a.x + o));
     }
-    // exclusive scan over experts of (passes, unique flag); lane owns a contiguous run
-    const int run = cdiv(E, 32);
-    const int e0 = min(E, lane * run), e1 = min(E, e0 + run);
-    int np = 0, nu = 0;
-    for (int ee = e0; ee < e1; ++ee) {
-      np += cdiv(s_cnt[ee], pmax);
-      nu += s_cnt[ee] > 0;
-    }
-    int inp = np, inu = nu;
+    *reinterpret_cast<uint2*>(xs + o) = v;
+  }
+  for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
+  __syncthreads();
+  if (live) {
+    float keep = 0.f;
+    for (int t = 0; t < T; ++t) {
+      const uint16_t* xr = xs + (size_t)t * H;
+      float acc = 0.f;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a1 = __shfl_up_sync(0xffffffffu, inp, o);
-      const int a2 = __shfl_up_sync(0xffffffffu, inu, o);
-      if (lane >= o) { inp += a1; inu += a2; }
+      for (int i = 0; i < RSW / 128; ++i) {
+        const int h = h0 + 4 * (lane + 32 * i);
+        uint2 xb = make_uint2(0u, 0u);
+        if (h < H) xb = *reinterpret_cast<const uint2*>(xr + h);
+        acc = fmaf(wv[i].x, __uint_as_float(xb.x << 16), acc);
+        acc = fmaf(wv[i].y, __uint_as_float(xb.x & 0xffff0000u), acc);
+        acc = fmaf(wv[i].z, __uint_as_float(xb.y << 16), acc);
+        acc = fmaf(wv[i].w, __uint_as_float(xb.y & 0xffff0000u), acc);
+      }
+      acc = warp_sum(acc);
+      if (lane == t) keep = acc;
     }
-    int off = inp - np, uoff = inu - nu;
-    for (int ee = e0; ee < e1; ++ee) {
-      s_off[ee] = off;
-      const int c = s_cnt[ee];
-      if (c > 0) a.plan.uniq[uoff++] = ee;
-      off += cdiv(c, pmax);
-    }
-    const int tot_p = __shfl_sync(0xffffffffu, inp, 31);
-    const int tot_u = __shfl_sync(0xffffffffu, inu, 31);
-    if (lane == 0) {
-      const int nsh = a.has_shared ? cdiv(T, pmax) : 0;
-      a.plan.hdr->n_pass = tot_p + nsh;
-      a.plan.hdr->n_routed_pass = tot_p;
-      a.plan.hdr->n_uniq = tot_u;
-      a.plan.hdr->T = T;
-      s_routed = tot_p;
-      DevCounters* dc = a.counters;
-      atomicAdd(&dc->forwards, 1ull);
-      atomicAdd(&dc->tokens, (unsigned long long)T);
-      atomicAdd(&dc->lookups, (unsigned long long)tot_u);
-      atomicAdd(&dc->bytes_touched, (unsigned long long)(tot_u + (a.has_shared ? 1 : 0)) * a.record_bytes);
-      atomicAdd(&dc->bytes_router, (unsigned long long)E * a.H * 4ull);
-    }
+    if (lane < T) spart[((size_t)lane * E + e) * NS + sl] = keep;
   }
   __syncthreads();
-
-  // ---------------- phase 2c: pass tables
-  const int routed_passes = s_routed;
-  for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
-    const int c = s_cnt[ee];
-    for (int i = 0; i * pmax < c; ++i) {
-      a.plan.pass_expert[s_off[ee] + i] = ee;
-      a.plan.pass_ntok[s_off[ee] + i] = min(pmax, c - i * pmax);
-    }
+  for (int q = threadIdx.x; q < T * E; q += blockDim.x) {
+    float v = 0.f;
+    for (int ss = 0; ss < NS; ++ss) v += spart[(size_t)q * NS + ss];
+    slog[q] = v;
   }
-  for (int q = threadIdx.x; q < T * k; q += blockDim.x) {
-    const int ee = s_idx[q], pos = s_pos[q];
-    const int pass = s_off[ee] + pos / pmax, slot = pos % pmax;
-    a.plan.pass_tok[pass * pmax + slot] = q / k;
-    a.plan.pair_pass[q] = pass;
-    a.plan.pair_slot[q] = slot;
-  }
-  if (a.has_shared) {
-    for (int t = threadIdx.x; t < T; t += blockDim.x) {
-      const int pass = routed_passes + t / pmax, slot = t % pmax;
-      a.plan.pass_tok[pass * pmax + slot] = t;
-      a.plan.shared_pass[t] = pass;
-      a.plan.shared_slot[t] = slot;
-      if (slot == 0) {
-        a.plan.pass_expert[pass] = E;
-        a.plan.pass_ntok[pass] = min(pmax, T - t);
-      }
-    }
-  }
-  // dense groups (pmax == 1: one pass per token): experts with >= big_min tokens go to the
-  // tcgen05 path in balanced chunks of <= GEMM_MAX_TOKENS, every other pass to the
-  // per-token path, both lists in ascending expert id (the shared expert last) then token
-  // order.  Warp 0: lane owns a contiguous run of experts, an exclusive scan places it.
-  if (warp == 0) {
-    if (a.big_min > 0) {
-      const int E1 = E + (a.has_shared ? 1 : 0);
-      const int run = cdiv(E1, 32);
-      const int e0 = min(E1, lane * run), e1 = min(E1, e0 + run);
-      auto cnt_of = [&](int ee) { return ee < E ? s_cnt[ee] : T; };
-      auto first_of = [&](int ee) { return ee < E ? s_off[ee] : routed_passes; };
-      int nb = 0, ns = 0;
-      for (int ee = e0; ee < e1; ++ee) {
-        const int c = cnt_of(ee), nc = big_chunks(c, a.big_min);
-        nb += nc;
-        ns += nc ? 0 : c;
-      }
-      int ib = nb, is = ns;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int a1 = __shfl_up_sync(0xffffffffu, ib, o);
-        const int a2 = __shfl_up_sync(0xffffffffu, is, o);
-        if (lane >= o) { ib += a1; is += a2; }
-      }
-      int ob = ib - nb, os = is - ns;
-      for (int ee = e0; ee < e1; ++ee) {
-        const int c = cnt_of(ee), first = first_of(ee), nc = big_chunks(c, a.big_min);
-        if (nc) {
-          const int base = c / nc, rem = c % nc;
-          int start = 0;
-          for (int q = 0; q < nc; ++q) {
-            const int sz = base + (q < rem ? 1 : 0);
-            a.plan.big[3 * ob + 0] = ee;
-            a.plan.big[3 * ob + 1] = first + start;
-            a.plan.big[3 * ob + 2] = sz;
-            ++ob;
-            start += sz;
-          }
-        } else {
-          for (int i = 0; i < c; ++i) a.plan.small_order[os++] = first + i;
-        }
-      }
-      if (lane == 31) {
-        a.plan.hdr->n_big = ib;
-        a.plan.hdr->n_small = is;
-      }
-    } else if (lane == 0) {
-      a.plan.hdr->n_big = 0;
-      a.plan.hdr->n_small = routed_passes + (a.has_shared ? cdiv(T, pmax) : 0);
-    }
-    if (lane == 0) *a.ticket = 0u;  // ready for the next launch (stream-ordered)
-  }
+  __syncthreads();
+  router_finish(a, slog, false, s_cnt, s_off, s_idx, s_pos, &s_routed);
 }
 
 cudaError_t router_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(router_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
 }
@@ -443,6 +561,8 @@ size_t router_smem_bytes(int H, int T, int E, int k) {
 }
 
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s) {
+  if (router_small_fits(a.H, a.T, a.E))
+    return launch_pdl(router_small_kernel, 1, RSMALL_THREADS, router_small_smem(a.H, a.T, a.E, a.k), s, a);
   const int grid = cdiv(a.H, RSW) * cdiv(a.E, REPB);
   const size_t smem = router_smem_bytes(a.H, a.T, a.E, a.k);
   if (grid > 2 * num_sms) return launch_pdl(router_kernel<3>, grid, 256, smem, s, a);

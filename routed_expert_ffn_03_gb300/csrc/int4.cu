@@ -316,7 +316,9 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
       if (++irb == ntask) { irb = 0; ++ipi; }
     }
   };
-  while (j_issue < min(D, nw)) issue_next();
+  // one copy per warp now, the rest of the ring after the fragments are built: a full
+  // ring's worth of copies queued at once makes each issue wait behind the others
+  if (j_issue < min(1, nw)) issue_next();
 
   const int gq = lane >> 2, p = lane & 3;
   const uint8_t* myring = smem + warp * D * I4_STAGE;
@@ -343,6 +345,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_gateup_kernel(ExpertArgs a) {
       }
       named_sync(1, nthr);
     }
+    while (j_issue < min(D, nw)) issue_next();
     float* part = a.part_gu + (size_t)pass * 2 * nks * I4_PMAX * rows32;
     const uint2* xcol = xfrag + i4_lane_col(lane, nb) * i4_kstride(a.H / 16);
     int local = ti - pi * per_pass;          // compute cursor within the pass

@@ -21,14 +21,15 @@ __global__ void __launch_bounds__(CB_ROWS * CB_KL) combine_kernel(CombineArgs a)
   __shared__ float red[CB_KL][CB_MAXJ][CB_ROWS];
   __shared__ long long s_base[CB_MAXJ];
   __shared__ float s_w[CB_MAXJ];
-  pdl_wait();  // part_d and the plan come from the kernels before
-  pdl_launch_dependents();
   const int t = blockIdx.y;
   const int rl = threadIdx.x & (CB_ROWS - 1), kl = threadIdx.x / CB_ROWS;
   const int r = blockIdx.x * CB_ROWS + rl;
   const int rows32 = cdiv(a.H, 32) * 32;
   const size_t slot_stride = rows32, ks_stride = (size_t)a.pmax * rows32;
   const int nj = a.k + (a.has_shared ? 1 : 0);
+  // The plan entries come from the router, which finished before the expert kernels ran
+  // (each of them waited for its predecessor), so they are read before the wait; the
+  // down partials are read after it.
   if (threadIdx.x < nj) {
     const int j = threadIdx.x;
     int pass, slot;
@@ -44,6 +45,8 @@ __global__ void __launch_bounds__(CB_ROWS * CB_KL) combine_kernel(CombineArgs a)
     s_base[j] = (long long)pass * a.nks_d * ks_stride + (long long)slot * slot_stride;
   }
   for (int j = 0; j < nj; ++j) red[kl][j][rl] = 0.f;
+  pdl_wait();  // part_d comes from the kernels before
+  pdl_launch_dependents();
   __syncthreads();
   const int nper = kl < a.nks_d ? cdiv(a.nks_d - kl, CB_KL) : 0;   // slices of this lane per expert
   const int U = r < a.H ? nj * nper : 0;

@@ -150,43 +150,79 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 namespace moe {
 // 1 / sqrt(mean((x + y)^2) + eps) over one row of H values (y may be null; H % 4 == 0,
-// rows 16-byte aligned), reduced in a fixed order (thread-strided float4 partial sums,
-// then warp and block trees), so every block that calls it on the same row gets the same
-// bits.  All threads of the block call it; red needs 32 floats.
+// rows 16-byte aligned), reduced in a fixed order that depends only on NTHR, the logical
+// thread count (the first NTHR threads hold data): thread i sums float4s i, i + NTHR, ...
+// in batches of 8, then warp trees, then a tree over the NTHR / 32 warps.  Every caller
+// uses the same NTHR, so every kernel that takes this norm of a row gets the same bits.
+// All threads of the block call it; red needs 32 floats.
+constexpr int RMS_NTHR = 256;
 __device__ __forceinline__ float block_inv_rms(const float* x, const float* y, int H, float eps, float* red) {
   float ss = 0.f;
-  const int step = blockDim.x, n4 = H >> 2;
+  const int n4 = H >> 2;
   const float4* x4 = reinterpret_cast<const float4*>(x);
   const float4* y4 = reinterpret_cast<const float4*>(y);
-  for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * step) {  // 8 (x, y) float4 loads in flight, summed in order
-    float4 v[8];
+  if ((int)threadIdx.x < RMS_NTHR) {
+    for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * RMS_NTHR) {  // 8 (x, y) float4 loads in flight, summed in order
+      float4 v[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int i = i0 + q * step;
-      v[q] = i < n4 ? __ldcg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-      if (y && i < n4) {
-        const float4 b = __ldcg(y4 + i);
-        v[q].x += b.x; v[q].y += b.y; v[q].z += b.z; v[q].w += b.w;
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * RMS_NTHR;
+        v[q] = i < n4 ? __ldcg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (y && i < n4) {
+          const float4 b = __ldcg(y4 + i);
+          v[q].x += b.x; v[q].y += b.y; v[q].z += b.z; v[q].w += b.w;
+        }
       }
-    }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      ss = fmaf(v[q].x, v[q].x, ss);
-      ss = fmaf(v[q].y, v[q].y, ss);
-      ss = fmaf(v[q].z, v[q].z, ss);
-      ss = fmaf(v[q].w, v[q].w, ss);
+      for (int q = 0; q < 8; ++q) {
+        ss = fmaf(v[q].x, v[q].x, ss);
+        ss = fmaf(v[q].y, v[q].y, ss);
+        ss = fmaf(v[q].z, v[q].z, ss);
+        ss = fmaf(v[q].w, v[q].w, ss);
+      }
     }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) red[warp] = ss;
+  if (lane == 0 && warp < RMS_NTHR / 32) red[warp] = ss;
   __syncthreads();
   if (warp == 0) {
-    float v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+    float v = lane < RMS_NTHR / 32 ? red[lane] : 0.f;
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / (float)H + eps);
+  __syncthreads();
+  return inv;
+}
+
+// block_inv_rms on values already in registers: for a thread i < RMS_NTHR, v[q] is float4
+// i + q * RMS_NTHR of the row (zero past the row; NV <= 8, so H <= 32 * RMS_NTHR), the same
+// elements and order as block_inv_rms, so the same bits.
+template <int NV>
+__device__ __forceinline__ float block_inv_rms_regs(const float4 (&v)[NV], int H, float eps, float* red) {
+  static_assert(NV <= 8, "one batch");
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < NV; ++q) {
+    ss = fmaf(v[q].x, v[q].x, ss);
+    ss = fmaf(v[q].y, v[q].y, ss);
+    ss = fmaf(v[q].z, v[q].z, ss);
+    ss = fmaf(v[q].w, v[q].w, ss);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0 && warp < RMS_NTHR / 32) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float w = lane < RMS_NTHR / 32 ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+    if (lane == 0) red[0] = w;
   }
   __syncthreads();
   const float inv = rsqrtf(red[0] / (float)H + eps);

@@ -455,6 +455,8 @@ size_t router_small_smem(int H, int T, int E, int k) {
          (size_t)(2 * E + 2 * T * k) * sizeof(int);
 }
 
+// V4: float4s of a row each norm thread holds in registers (H <= 4 * RMS_NTHR * V4)
+template <int V4>
 __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs a) {
   extern __shared__ __align__(16) int sm[];
   __shared__ float s_inv[ROUTER_FUSED_MAXT];
@@ -485,34 +487,70 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
   }
   pdl_wait();  // x (and the residual) come from the kernels before
   pdl_launch_dependents();
-  if (fused) {
+  if (fused && H <= RMS_NTHR * V4 * 4) {
+    // one pass over x + y_prev: the first RMS_NTHR threads keep their float4s of a row in
+    // registers for both the norm (block_inv_rms_regs: the order of block_inv_rms) and the
+    // staging
     for (int t = 0; t < T; ++t) {
-      const float inv = block_inv_rms(a.xres + (size_t)t * H, a.yprev ? a.yprev + (size_t)t * H : nullptr, H,
-                                      a.eps, s_red);
-      if (threadIdx.x == 0) s_inv[t] = inv;
-    }
-    __syncthreads();
-  }
-  for (int q = threadIdx.x; q < T * (H / 4); q += blockDim.x) {
-    const int t = q / (H / 4), h = 4 * (q - t * (H / 4));
-    const size_t o = (size_t)t * H + h;
-    uint2 v;
-    if (fused) {
-      float4 x4 = __ldcg(reinterpret_cast<const float4*>(a.xres + o));
-      if (a.yprev) {
-        const float4 y4 = __ldcg(reinterpret_cast<const float4*>(a.yprev + o));
-        x4.x += y4.x; x4.y += y4.y; x4.z += y4.z; x4.w += y4.w;
+      const size_t ro = (size_t)t * H;
+      float4 v[V4];
+#pragma unroll
+      for (int q = 0; q < V4; ++q) {
+        const int i = threadIdx.x + q * RMS_NTHR;
+        v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if ((int)threadIdx.x < RMS_NTHR && i < H / 4) {
+          v[q] = __ldcg(reinterpret_cast<const float4*>(a.xres + ro) + i);
+          if (a.yprev) {
+            const float4 y4 = __ldcg(reinterpret_cast<const float4*>(a.yprev + ro) + i);
+            v[q].x += y4.x; v[q].y += y4.y; v[q].z += y4.z; v[q].w += y4.w;
+          }
+        }
       }
-      const float inv = s_inv[t];
-      v.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.x * inv)) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.y * inv)) << 16);
-      v.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.z * inv)) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.w * inv)) << 16);
-      *reinterpret_cast<uint2*>(a.xn_out + o) = v;
-    } else {
-      v = __ldg(reinterpret_cast<const uint2*>(a.x + o));
+      const float inv = block_inv_rms_regs<V4>(v, H, a.eps, s_red);
+#pragma unroll
+      for (int q = 0; q < V4; ++q) {
+        const int i = threadIdx.x + q * RMS_NTHR;
+        if ((int)threadIdx.x < RMS_NTHR && i < H / 4) {
+          uint2 o;
+          o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[q].x * inv)) |
+                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[q].y * inv)) << 16);
+          o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[q].z * inv)) |
+                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[q].w * inv)) << 16);
+          *reinterpret_cast<uint2*>(a.xn_out + ro + 4 * i) = o;
+          *reinterpret_cast<uint2*>(xs + ro + 4 * i) = o;
+        }
+      }
     }
-    *reinterpret_cast<uint2*>(xs + o) = v;
+  } else {
+    if (fused) {
+      for (int t = 0; t < T; ++t) {
+        const float inv = block_inv_rms(a.xres + (size_t)t * H, a.yprev ? a.yprev + (size_t)t * H : nullptr, H,
+                                        a.eps, s_red);
+        if (threadIdx.x == 0) s_inv[t] = inv;
+      }
+      __syncthreads();
+    }
+    for (int q = threadIdx.x; q < T * (H / 4); q += blockDim.x) {
+      const int t = q / (H / 4), h = 4 * (q - t * (H / 4));
+      const size_t o = (size_t)t * H + h;
+      uint2 v;
+      if (fused) {
+        float4 x4 = __ldcg(reinterpret_cast<const float4*>(a.xres + o));
+        if (a.yprev) {
+          const float4 y4 = __ldcg(reinterpret_cast<const float4*>(a.yprev + o));
+          x4.x += y4.x; x4.y += y4.y; x4.z += y4.z; x4.w += y4.w;
+        }
+        const float inv = s_inv[t];
+        v.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.x * inv)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.y * inv)) << 16);
+        v.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.z * inv)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.w * inv)) << 16);
+        *reinterpret_cast<uint2*>(a.xn_out + o) = v;
+      } else {
+        v = __ldg(reinterpret_cast<const uint2*>(a.x + o));
+      }
+      *reinterpret_cast<uint2*>(xs + o) = v;
+    }
   }
   for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
   __syncthreads();
@@ -549,7 +587,9 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
 cudaError_t router_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(router_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  e = cudaFuncSetAttribute(router_small_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(router_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
 }
@@ -561,8 +601,11 @@ size_t router_smem_bytes(int H, int T, int E, int k) {
 }
 
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s) {
-  if (router_small_fits(a.H, a.T, a.E))
-    return launch_pdl(router_small_kernel, 1, RSMALL_THREADS, router_small_smem(a.H, a.T, a.E, a.k), s, a);
+  if (router_small_fits(a.H, a.T, a.E)) {
+    const size_t smem = router_small_smem(a.H, a.T, a.E, a.k);
+    if (a.H <= 4 * RMS_NTHR * 4) return launch_pdl(router_small_kernel<4>, 1, RSMALL_THREADS, smem, s, a);
+    return launch_pdl(router_small_kernel<8>, 1, RSMALL_THREADS, smem, s, a);
+  }
   const int grid = cdiv(a.H, RSW) * cdiv(a.E, REPB);
   const size_t smem = router_smem_bytes(a.H, a.T, a.E, a.k);
   if (grid > 2 * num_sms) return launch_pdl(router_kernel<3>, grid, 256, smem, s, a);

@@ -167,7 +167,12 @@ def test_bounded_device_wait_reports_timeout():
     ctx.close()
 
 
-@pytest.mark.parametrize("spec", [SPEC, SPEC4])
+# wide rows: the single-block router (8 experts x 4 slices) and the multi-block one (16 x 7)
+SPEC_H4K = LayerSpec(4096, 256, 8, 2, S.INT4, router=0, seed=23, layers=2)
+SPEC_H7K = LayerSpec(7168, 256, 16, 4, S.RVQ, router=0, seed=24, layers=2)
+
+
+@pytest.mark.parametrize("spec", [SPEC, SPEC4, SPEC_H4K, SPEC_H7K])
 def test_fused_stack_step_equals_separate_calls(spec):
     """moe_forward_residual == moe_residual_rmsnorm + moe_forward, bit for bit."""
     import torch

@@ -46,16 +46,19 @@ constexpr int I4_STATIC_SMEM = I4_MAX_RECS * 8 + 128;
 // load phase are conflict-free).
 __host__ __device__ constexpr int i4_kstride(int nks16) { return nks16 + 2; }
 
+constexpr int DN_UMAX = 2;   // units (pass, k-slice) a down block prepares up front
+
 // nb = mma columns that carry data (2 per token of the widest pass).
 template <int NW, int D>
 struct I4Smem {
   static constexpr int ring = NW * D * I4_STAGE;
   static constexpr int bars = NW * D * 8;
   static constexpr int gateup(int H, int nb) { return ring + bars + nb * 4 * i4_kstride(H / 16) * 8; }
-  // down keeps B fragments for all 8 columns (one slice is small) and the slice inputs
-  static constexpr int down() {
-    return ring + bars + 8 * 4 * i4_kstride(I4_SLICE_KSTEPS) * 8 + I4_PMAX * I4_KS * I4_GROUP * 4;
-  }
+  // down keeps, for each of up to DN_UMAX units, B fragments for all 8 columns (one slice
+  // is small) and the slice inputs
+  static constexpr int dn_frag = 8 * 4 * i4_kstride(I4_SLICE_KSTEPS) * 8;
+  static constexpr int dn_vin = I4_PMAX * I4_KS * I4_GROUP * 4;
+  static constexpr int down() { return ring + bars + DN_UMAX * (dn_frag + dn_vin); }
 };
 
 __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
@@ -393,8 +396,10 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
   __shared__ const uint8_t* s_rec[I4_MAX_RECS];
   using SM = I4Smem<NW, D>;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::ring);
+  // unit slot ui: B fragments at xfrag + ui * DFRAG, inputs at vin + ui * DVIN
+  constexpr int DFRAG = SM::dn_frag / 8, DVIN = SM::dn_vin / 4;
   uint2* xfrag = reinterpret_cast<uint2*>(smem + SM::ring + SM::bars);
-  float* vin = reinterpret_cast<float*>(smem + SM::ring + SM::bars + 8 * 4 * i4_kstride(I4_SLICE_KSTEPS) * 8);
+  float* vin = reinterpret_cast<float*>(smem + SM::ring + SM::bars + DN_UMAX * SM::dn_frag);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars + warp * D);
   const uint32_t ring0 = smem_u32(smem + warp * D * I4_STAGE);
@@ -462,59 +467,100 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
   int cslot = 0;
   uint32_t cphase = 0u;
   int ti = first;
+  // h of a unit's slice: silu(g) * u, the gate / up partials added in k-slice order
+  auto unit_h = [&](int pass, int ts, int kbase, int kk, int kvalid) {
+    float v = 0.f;
+    if (kk < kvalid) {
+      const size_t stride = (size_t)I4_PMAX * rows32_f;
+      const float* pg = a.part_gu + ((size_t)pass * 2 * nks_gu * I4_PMAX + ts) * rows32_f + kbase + kk;
+      const float* pu = pg + (size_t)nks_gu * stride;
+      float gs = 0.f, us = 0.f;
+      for (int s0 = 0; s0 < nks_gu; s0 += 16) {   // 32 loads in flight, added in slice order
+        float gv[16], uv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const bool in = s0 + q < nks_gu;
+          gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * stride) : 0.f;
+          uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * stride) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          if (s0 + q < nks_gu) {
+            gs += gv[q];
+            us += uv[q];
+          }
+        }
+      }
+      v = gs / (1.f + expf(-gs)) * us;
+    }
+    return v;
+  };
+  struct DnUnit {
+    int pass, ks, ntok, ng;
+  };
+  auto unit_at = [&](int u) {
+    DnUnit U;
+    const int pi = u / nks;
+    U.ks = u - pi * nks;
+    U.pass = pass_of(a, p_begin, pi);
+    U.ntok = a.T == 1 ? 1 : __ldcg(a.plan.pass_ntok + U.pass);
+    U.ng = min(I4_KS, NG - U.ks * I4_KS);
+    return U;
+  };
+  // A block's range covers one or two units: both are prepared up front, their inputs
+  // read in one round trip, so the warps then run through their tasks without a barrier.
+  // A block with more units prepares each when it reaches it.
+  const int u_first = t0 / ntask, n_units = (t1 - 1) / ntask - u_first + 1;
+  const bool pre = n_units <= DN_UMAX;
+  if (pre) {
+    DnUnit U0 = unit_at(u_first), U1 = U0;
+    if (n_units > 1) U1 = unit_at(u_first + 1);
+    const int e0 = U0.ntok * I4_KS * I4_GROUP, e1 = n_units > 1 ? U1.ntok * I4_KS * I4_GROUP : 0;
+    for (int q = threadIdx.x; q < e0 + e1; q += nthr) {
+      const bool second = q >= e0;
+      const DnUnit& U = second ? U1 : U0;
+      const int e = second ? q - e0 : q;
+      const int ts = e / (I4_KS * I4_GROUP), kk = e - ts * (I4_KS * I4_GROUP);
+      vin[(second ? DVIN : 0) + e] = unit_h(U.pass, ts, U.ks * I4_KS * I4_GROUP, kk, U.ng * I4_GROUP);
+    }
+    named_sync(1, nthr);
+    build_bfrags(xfrag, I4_SLICE_KSTEPS, 2 * U0.ntok, threadIdx.x, nthr,
+                 [&](int ts, int k) { return vin[ts * (I4_KS * I4_GROUP) + k]; });
+    if (n_units > 1)
+      build_bfrags(xfrag + DFRAG, I4_SLICE_KSTEPS, 2 * U1.ntok, threadIdx.x, nthr,
+                   [&](int ts, int k) { return vin[DVIN + ts * (I4_KS * I4_GROUP) + k]; });
+    named_sync(1, nthr);
+    while (j_issue < min(D, nw)) issue_next();
+  }
   for (int seg = t0; seg < t1;) {  // segments = one unit (pass, k-slice) each
     const int u = seg / ntask;
     const int seg_end = min(t1, (u + 1) * ntask);
-    const int pi = u / nks, ks = u - pi * nks;
-    const int pass = pass_of(a, p_begin, pi);
-    const int ntok = a.T == 1 ? 1 : __ldcg(a.plan.pass_ntok + pass);
-    const int nb = 2 * ntok;
-    const int ng = min(I4_KS, NG - ks * I4_KS);
-    const int kbase = ks * I4_KS * I4_GROUP, kvalid = ng * I4_GROUP;
-    named_sync(1, nthr);
-    // h of this slice: silu(g) * u, the gate / up partials added in k-slice order
-    for (int e = threadIdx.x; e < ntok * I4_KS * I4_GROUP; e += nthr) {
-      const int ts = e / (I4_KS * I4_GROUP), kk = e - ts * (I4_KS * I4_GROUP);
-      float v = 0.f;
-      if (kk < kvalid) {
-        const size_t stride = (size_t)I4_PMAX * rows32_f;
-        const float* pg = a.part_gu + ((size_t)pass * 2 * nks_gu * I4_PMAX + ts) * rows32_f + kbase + kk;
-        const float* pu = pg + (size_t)nks_gu * stride;
-        float gs = 0.f, us = 0.f;
-        for (int s0 = 0; s0 < nks_gu; s0 += 16) {   // 32 loads in flight, added in slice order
-          float gv[16], uv[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const bool in = s0 + q < nks_gu;
-            gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * stride) : 0.f;
-            uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * stride) : 0.f;
-          }
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            if (s0 + q < nks_gu) {
-              gs += gv[q];
-              us += uv[q];
-            }
-          }
-        }
-        v = gs / (1.f + expf(-gs)) * us;
+    const DnUnit U = unit_at(u);
+    const int nb = 2 * U.ntok;
+    int slot_u = 0;
+    if (pre) {
+      slot_u = u - u_first;
+    } else {
+      named_sync(1, nthr);
+      for (int e = threadIdx.x; e < U.ntok * I4_KS * I4_GROUP; e += nthr) {
+        const int ts = e / (I4_KS * I4_GROUP), kk = e - ts * (I4_KS * I4_GROUP);
+        vin[e] = unit_h(U.pass, ts, U.ks * I4_KS * I4_GROUP, kk, U.ng * I4_GROUP);
       }
-      vin[e] = v;
+      named_sync(1, nthr);
+      build_bfrags(xfrag, I4_SLICE_KSTEPS, nb, threadIdx.x, nthr,
+                   [&](int ts, int k) { return vin[ts * (I4_KS * I4_GROUP) + k]; });
+      named_sync(1, nthr);
+      while (j_issue < min(D, nw)) issue_next();
     }
-    named_sync(1, nthr);
-    build_bfrags(xfrag, I4_SLICE_KSTEPS, nb, threadIdx.x, nthr,
-                 [&](int ts, int k) { return vin[ts * (I4_KS * I4_GROUP) + k]; });
-    named_sync(1, nthr);
-    while (j_issue < min(D, nw)) issue_next();
-    float* dst0 = a.part_d + ((size_t)pass * nks + ks) * I4_PMAX * rows32;
-    const uint2* xcol = xfrag + i4_lane_col(lane, nb) * i4_kstride(I4_SLICE_KSTEPS);
+    float* dst0 = a.part_d + ((size_t)U.pass * nks + U.ks) * I4_PMAX * rows32;
+    const uint2* xcol = xfrag + slot_u * DFRAG + i4_lane_col(lane, nb) * i4_kstride(I4_SLICE_KSTEPS);
     for (; ti < seg_end; ti += NW) {
       const int rb = ti - u * ntask;
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const bool ok = stage_wait(full0 + 8 * cslot, cphase, &s_abort, a, lane);
       if (ok) {
         const uint8_t* st = myring + cslot * I4_STAGE;
-        if (ng == 2) i4_task<2>(st + lane * 16, st + 1024 + gq * 4, xcol, acc);
+        if (U.ng == 2) i4_task<2>(st + lane * 16, st + 1024 + gq * 4, xcol, acc);
         else i4_task<1>(st + lane * 16, st + 1024 + gq * 4, xcol, acc);
       }
       __syncwarp();
@@ -524,7 +570,7 @@ __global__ void __launch_bounds__(NW * 32, 1) int4_down_kernel(ExpertArgs a) {
         cphase ^= 1u;
       }
       if (ok && j_issue < nw) issue_next();
-      if (ok && p < ntok) {
+      if (ok && p < U.ntok) {
         float* dst = dst0 + (size_t)p * rows32 + rb * 32;
         dst[gq] = acc[0][0] + acc[0][1];
         dst[gq + 8] = acc[0][2] + acc[0][3];
@@ -544,6 +590,11 @@ struct I4Launch {
   int nw, d;
   size_t smem_gu, smem_down;
 };
+
+// every configuration's down kernel fits whatever the shapes (its shared memory does not
+// depend on them)
+static_assert(I4Smem<24, 2>::down() <= 227 * 1024 - I4_STATIC_SMEM, "down smem");
+static_assert(I4Smem<16, 3>::down() <= 227 * 1024 - I4_STATIC_SMEM, "down smem");
 
 static I4Launch i4_config(int H, int max_tokens) {
   const int nb = 2 * std::min(max_tokens, I4_PMAX);

@@ -8,10 +8,12 @@
 // activations enter as fp16 hi + lo columns (n = 2 token + part), so all products are
 // exact and the three stages and all k accumulate in fp32 in tensor memory.
 //
-// Work item = (group of <= 32 tokens of one expert, matrix, 512-input k-slice, 128-row
-// tile).  A block (8 warps) takes items round-robin.  Per item: one bulk TMA copy each of
-// the matrix's codebooks (12 KB) and the tile's codes (4 row blocks x 6 KB); the B
-// operand (X hi/lo, K-major canonical layout, no swizzle) is built once; then for each of
+// Work item = (group of <= 32 tokens of one expert, 512-input k-slice, matrix, 128-row
+// tile), in that order; a block (8 warps) takes an equal contiguous range of items, so
+// its consecutive items share the group and k-slice and the B operand (X hi/lo, K-major
+// canonical layout, no swizzle, built from 16-byte loads) is built once for them.  Per
+// item: one bulk TMA copy each of the matrix's codebooks (12 KB) and the tile's codes
+// (4 row blocks x 6 KB); then for each of
 // the 8 k-blocks of 64 inputs the block gathers the three A stage tiles (128 x 64 fp16
 // each, K-major canonical layout) into one of two buffers and one thread issues
 // 3 x 4 tcgen05.mma (M = 128, N = 16..64, K = 16) into the TMEM accumulator, committing
@@ -123,7 +125,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
 
   const int n_big = __ldcg(&a.plan.hdr->n_big);
   const int total = n_big * mats * nks * ntile;
-  if (blockIdx.x >= total) return;  // uniform across the block: no tensor memory taken
+  const int it0 = (int)((long long)total * blockIdx.x / gridDim.x);
+  const int it1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+  if (it0 >= it1) return;  // no item for this block (uniform): no tensor memory taken
 
   if (tid == 0) {
     mbar_init(bar_tma, 1);
@@ -144,14 +148,16 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
   const uint32_t tmem = *tmem_slot;
 
   int tma_phase = 0, mma_phase[2] = {0, 0}, mma_pending[2] = {0, 0};
-  for (int it = blockIdx.x; it < total && !s_abort; it += gridDim.x) {
+  __shared__ int s_tok[GEMM_MAX_TOKENS];
+  int b_grp = -1, b_ks = -1;    // the group and k-slice the B operand holds
+  for (int it = it0; it < it1 && !s_abort; ++it) {
     GmItem I;
     I.tile = it % ntile;
     int rest = it / ntile;
-    I.ks = rest % nks;
-    rest /= nks;
     I.m = rest % mats;
-    I.grp = rest / mats;
+    rest /= mats;
+    I.ks = rest % nks;
+    I.grp = rest / nks;
     const int expert = __ldcg(a.plan.big + 3 * I.grp + 0);
     const int pass0 = __ldcg(a.plan.big + 3 * I.grp + 1);
     const int ntok = __ldcg(a.plan.big + 3 * I.grp + 2);
@@ -168,31 +174,61 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
       bulk_g2s(smem_u32(codes), mat + GM_CB + ((size_t)I.ks * g.ntask + rb0) * RVQ_TASK_BYTES,
                nrb * RVQ_TASK_BYTES, bar_tma);
     }
-    // B operand: column n = 2 t + part of token t of the group, K-major canonical layout
-    const int kbase = I.ks * RVQ_KS * RVQ_GROUP;
-    for (int e = tid; e < N * (RVQ_KS * RVQ_GROUP / 2); e += GM_THREADS) {
-      const int n = e / (RVQ_KS * RVQ_GROUP / 2), kp = e - n * (RVQ_KS * RVQ_GROUP / 2);
-      const int k = 2 * kp;               // two inputs per thread step
-      const int t = n >> 1, part = n & 1;
-      float v0 = 0.f, v1 = 0.f;
-      if (t < ntok) {
-        const int pass = pass0 + t;
-        const int kk0 = kbase + k;
-        if (!DOWN) {
-          const int tok = __ldcg(a.plan.pass_tok + pass);
-          if (kk0 < g.K) v0 = bf16_bits_to_float(a.x[(size_t)tok * a.H + kk0]);
-          if (kk0 + 1 < g.K) v1 = bf16_bits_to_float(a.x[(size_t)tok * a.H + kk0 + 1]);
-        } else {
-          const float* hp = a.h + (size_t)pass * rows32_gu;   // SwiGLU of this pass (rvq_swiglu_big)
-          if (kk0 < g.K) v0 = __ldcg(hp + kk0);
-          if (kk0 + 1 < g.K) v1 = __ldcg(hp + kk0 + 1);
+    // B operand: column n = 2 t + part of token t of the group, K-major canonical layout;
+    // one thread step = 8 consecutive inputs of one token (hi and lo columns)
+    if (I.grp != b_grp || I.ks != b_ks) {
+      if (!DOWN && tid < ntok) s_tok[tid] = __ldcg(a.plan.pass_tok + pass0 + tid);
+      __syncthreads();
+      const int kbase = I.ks * RVQ_KS * RVQ_GROUP;
+      constexpr int C8 = RVQ_KS * RVQ_GROUP / 8;   // 64 chunks of 8 inputs per slice
+      for (int e = tid; e < (N / 2) * C8; e += GM_THREADS) {
+        const int t = e / C8, c8 = e - t * C8;
+        const int k = c8 * 8, kk0 = kbase + k;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        if (t < ntok) {
+          if (!DOWN) {
+            const uint16_t* xr = a.x + (size_t)s_tok[t] * a.H + kk0;
+            if (kk0 + 8 <= g.K) {
+              const uint4 u = __ldg(reinterpret_cast<const uint4*>(xr));
+              const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(w4[i] << 16);
+                v[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
+              }
+            } else {
+              for (int i = 0; i < 8; ++i)
+                if (kk0 + i < g.K) v[i] = bf16_bits_to_float(xr[i]);
+            }
+          } else {
+            const float* hp = a.h + (size_t)(pass0 + t) * rows32_gu + kk0;   // SwiGLU (rvq_swiglu_big)
+            if (kk0 + 8 <= g.K) {
+              const float4 f0 = __ldcg(reinterpret_cast<const float4*>(hp));
+              const float4 f1 = __ldcg(reinterpret_cast<const float4*>(hp) + 1);
+              v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w;
+              v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+            } else {
+              for (int i = 0; i < 8; ++i)
+                if (kk0 + i < g.K) v[i] = __ldcg(hp + i);
+            }
+          }
         }
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __half h0, l0, h1, l1;
+          split_half(v[2 * i], h0, l0);
+          split_half(v[2 * i + 1], h1, l1);
+          hw[i] = pack_half2(h0, h1);
+          lw[i] = pack_half2(l0, l1);
+        }
+        *reinterpret_cast<uint4*>(bsm + canon_off(2 * t, k, C8)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(bsm + canon_off(2 * t + 1, k, C8)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
-      __half h0, l0, h1, l1;
-      split_half(v0, h0, l0);
-      split_half(v1, h1, l1);
-      const uint32_t pk = part ? pack_half2(l0, l1) : pack_half2(h0, h1);
-      *reinterpret_cast<uint32_t*>(bsm + canon_off(n, k, RVQ_KS * RVQ_GROUP / 8)) = pk;
+      b_grp = I.grp;
+      b_ks = I.ks;
     }
     // the tile's codes must have landed before the gather
     bool ok = mbar_wait_bounded(bar_tma, tma_phase & 1, a.budget);

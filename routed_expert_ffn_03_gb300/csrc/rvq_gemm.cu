@@ -346,6 +346,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
 
 // h[pass][row] = silu(g) * u for the passes of the GEMM groups, g and u the gate / up
 // k-slice partials added in slice order (the same order the lookup-table down kernel uses).
+// One thread per (token of the group, row), its partial loads all in flight.
 __global__ void __launch_bounds__(256) rvq_swiglu_big_kernel(ExpertArgs a) {
   const RecGeom rg = rec_geom(WFMT_RVQ, a.H, a.F);
   const MatGeom gg = rg.m[0];
@@ -353,28 +354,30 @@ __global__ void __launch_bounds__(256) rvq_swiglu_big_kernel(ExpertArgs a) {
   const int grp = blockIdx.y;
   if (grp >= __ldcg(&a.plan.hdr->n_big)) return;
   const int pass0 = __ldcg(a.plan.big + 3 * grp + 1), ntok = __ldcg(a.plan.big + 3 * grp + 2);
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ntok * a.F; i += gridDim.x * blockDim.x) {
-    const int t = i / a.F, r = i - t * a.F;
-    const int pass = pass0 + t;
-    const float* pg = a.part_gu + ((size_t)(pass * 2 + 0) * gg.nks) * rows32 + r;
-    const float* pu = a.part_gu + ((size_t)(pass * 2 + 1) * gg.nks) * rows32 + r;
-    float gs = 0.f, us = 0.f;
-    for (int s0 = 0; s0 < gg.nks; s0 += 8) {
-      float gv[8], uv[8];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= ntok * a.F) return;
+  const int t = i / a.F, r = i - t * a.F;
+  const int pass = pass0 + t;
+  const float* pg = a.part_gu + ((size_t)(pass * 2 + 0) * gg.nks) * rows32 + r;
+  const float* pu = a.part_gu + ((size_t)(pass * 2 + 1) * gg.nks) * rows32 + r;
+  float gs = 0.f, us = 0.f;
+  for (int s0 = 0; s0 < gg.nks; s0 += 16) {
+    float gv[16], uv[16];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const bool in = s0 + q < gg.nks;
-        gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * rows32) : 0.f;
-        uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * rows32) : 0.f;
-      }
+    for (int q = 0; q < 16; ++q) {
+      const bool in = s0 + q < gg.nks;
+      gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * rows32) : 0.f;
+      uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * rows32) : 0.f;
+    }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 16; ++q) {
+      if (s0 + q < gg.nks) {
         gs += gv[q];
         us += uv[q];
       }
     }
-    a.h[(size_t)pass * rows32 + r] = gs / (1.f + expf(-gs)) * us;
   }
+  a.h[(size_t)pass * rows32 + r] = gs / (1.f + expf(-gs)) * us;
 }
 
 cudaError_t rvq_gemm_set_attributes() {
@@ -388,7 +391,7 @@ cudaError_t launch_rvq_gemm_gateup(const ExpertArgs& a, int grid, cudaStream_t s
   return cudaGetLastError();
 }
 cudaError_t launch_rvq_gemm_down(const ExpertArgs& a, int grid, cudaStream_t s, int max_big) {
-  dim3 sg(cdiv(a.F, 256), max_big);
+  dim3 sg(cdiv(GEMM_MAX_TOKENS * a.F, 256), max_big);
   rvq_swiglu_big_kernel<<<sg, 256, 0, s>>>(a);
   rvq_gemm_kernel<true><<<grid, GM_THREADS, GM_SMEM, s>>>(a);
   return cudaGetLastError();

@@ -44,6 +44,8 @@ def test_tiny_config_rvq_top2_softmax():
     (256, 136, 16, 4, 32, 0, True),     # T = 32 with shared expert (dense tcgen05 groups)
     (512, 384, 4, 2, 16, 1, True),      # T = 16: most experts take the dense path
     (264, 200, 3, 3, 40, 0, False),     # 40 tokens on every expert: split into 2 dense groups
+    (64, 48, 1, 1, 5, 1, False),        # a single expert, k = 1 (weight 1 for both score kinds)
+    (128, 96, 12, 3, 256, 0, True),     # the largest T (256): many dense groups, the two-level router
 ])
 def test_rvq_odd_shapes(H, F, E, k, T, router, shared):
     _run(LayerSpec(H, F, E, k, S.RVQ, router=router, shared=shared, seed=H + F + E), T)
@@ -55,6 +57,8 @@ def test_rvq_odd_shapes(H, F, E, k, T, router, shared):
     (512, 384, 9, 3, 3, 1, True),       # sigmoid + shared, T = 3
     (256, 256, 40, 4, 4, 0, False),     # one pass carries 4 tokens when they share an expert
     (256, 128, 8, 2, 32, 1, True),      # T = 32: experts with > 4 tokens take several passes
+    (128, 128, 1, 1, 3, 0, False),      # a single expert, k = 1
+    (256, 256, 12, 3, 256, 1, True),    # the largest T (256): up to 4 tokens per pass, many passes
 ])
 def test_int4_odd_shapes(H, F, E, k, T, router, shared):
     _run(LayerSpec(H, F, E, k, S.INT4, router=router, shared=shared, seed=H + F + E), T)

@@ -135,9 +135,23 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   bool waited = !DOWN;
   const int p_begin = a.range.p_begin;
   const int p_end = a.range.p_end >= 0 ? a.range.p_end : __ldcg(a.range.count ? a.range.count : &a.plan.hdr->n_pass);
-  const int total = max(0, p_end - p_begin) * mats * nks * ntask;
-  const int t0 = (int)((long long)total * blockIdx.x / gridDim.x);
-  const int t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+  const int n_units = max(0, p_end - p_begin) * mats * nks;
+  const int total = n_units * ntask;
+  // Work split.  Every unit (pass, matrix, k-slice) costs a table build, so with no more
+  // units than blocks each unit goes to its own group of blocks, which split its tasks:
+  // every block builds one table.  Otherwise blocks take equal contiguous task ranges.
+  int t0, t1;
+  if (n_units > 0 && n_units <= (int)gridDim.x) {
+    const int u = (int)((long long)blockIdx.x * n_units / gridDim.x);
+    const int b_lo = (int)(((long long)u * gridDim.x + n_units - 1) / n_units);
+    const int b_hi = (int)(((long long)(u + 1) * gridDim.x + n_units - 1) / n_units);
+    const int i = blockIdx.x - b_lo, n = b_hi - b_lo;
+    t0 = u * ntask + (int)((long long)ntask * i / n);
+    t1 = u * ntask + (int)((long long)ntask * (i + 1) / n);
+  } else {
+    t0 = (int)((long long)total * blockIdx.x / gridDim.x);
+    t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+  }
   const uint32_t l4 = (uint32_t)lane << 2;
   const uint32_t delta = smem_u32(smem) - RV_DYN_BASE;   // 0 on the fast path
 

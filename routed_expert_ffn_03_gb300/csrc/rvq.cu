@@ -139,9 +139,13 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   const int total = n_units * ntask;
   // Work split.  Every unit (pass, matrix, k-slice) costs a table build, so with no more
   // units than blocks each unit goes to its own group of blocks, which split its tasks:
-  // every block builds one table.  Otherwise blocks take equal contiguous task ranges.
+  // every block builds one table; with at least two units per block, blocks take whole
+  // units (contiguous unit ranges); in between, equal contiguous task ranges.
   int t0, t1;
-  if (n_units > 0 && n_units <= (int)gridDim.x) {
+  if (n_units >= 2 * (int)gridDim.x) {
+    t0 = (int)((long long)n_units * blockIdx.x / gridDim.x) * ntask;
+    t1 = (int)((long long)n_units * (blockIdx.x + 1) / gridDim.x) * ntask;
+  } else if (n_units > 0 && n_units <= (int)gridDim.x) {
     const int u = (int)((long long)blockIdx.x * n_units / gridDim.x);
     const int b_lo = (int)(((long long)u * gridDim.x + n_units - 1) / n_units);
     const int b_hi = (int)(((long long)(u + 1) * gridDim.x + n_units - 1) / n_units);

@@ -15,14 +15,19 @@
 // Phase 1 (all blocks): block (s, g) owns the 1024-wide slice s of H and the group g of
 // 8 experts, one per warp.  A warp loads its expert's slice of W into registers before
 // it waits on the kernel before (the weights do not depend on it), the block stages the
-// slice of the bf16 router input in shared memory, and the warp writes the partial dot
-// products of all T tokens.  The last block of a group to finish (an atomic ticket per
-// group) adds the group's partials in slice order into the logits; the last group to
-// finish (a second ticket) runs phase 2: the top-k per token (one warp per token,
-// straight from the logits) and the bucketing of the (token, rank) pairs by expert into
-// "passes" of up to pmax tokens: routed experts in ascending id, tokens ascending, then
-// the shared expert.  No block ever waits on another.
+// slice of the bf16 router input in shared memory, and the warp computes the partial dot
+// products of all T tokens.  The group's logits are its partials added in slice order:
+// with at most 8 slices the slice blocks of a group are one cluster and add them in
+// distributed shared memory (router_cluster_kernel), otherwise the last block of the
+// group (an atomic ticket per group) adds them from global memory (router_kernel).  The
+// last group to finish (a second ticket) runs phase 2: the top-k per token (one warp per
+// token, straight from the logits) and the bucketing of the (token, rank) pairs by
+// expert into "passes" of up to pmax tokens: routed experts in ascending id, tokens
+// ascending, then the shared expert.  Problems that fit one block use
+// router_small_kernel, with no global partials at all.
 #include <cfloat>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -32,14 +37,10 @@ namespace moe {
 constexpr int RSW = 1024;   // inputs per slice: 8 float4 of W per lane
 constexpr int REPB = 8;     // experts per block (one per warp)
 constexpr int RTG = 32;     // tokens staged per pass over the slice
-constexpr int RXS_BYTES = RTG * RSW * 2;
-constexpr int RNS_ONE = 8;                 // the last block adds the slices itself when
-constexpr size_t RSUM_ONE_BLOCK = 16384;   // NS <= RNS_ONE and NS * T * E <= RSUM_ONE_BLOCK
-__host__ __device__ __forceinline__ bool router_two_level(int NS, int T, int E) {
-  return NS > RNS_ONE || (size_t)NS * T * E > RSUM_ONE_BLOCK;
-}
 int router_nch(int H) { return cdiv(H, RSW) + 1; }     // slices of partials + the logits
 int router_tickets(int E) { return cdiv(E, REPB) + 1; }
+constexpr int RCAND = 64;   // candidates of a token ranked exactly (more: iterative selection)
+constexpr int RCAND_WARP = RCAND + 32;   // (logit, id) pairs per warp: candidates + the k selected
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -54,48 +55,100 @@ __device__ __forceinline__ int big_chunks(int c, int big_min) {
 
 // Top-k of one token's E logits (one warp; NV * 32 >= E values, lane l holds experts
 // l + 32 i), then the k weights; writes the plan's and the per-layer copy of the routing.
-// Each lane keeps the maximum of its own experts not yet taken; the warp takes the best k
-// times, and only the lane that gave its maximum away looks for its next one.  NaN ranks
-// as -inf; equal values rank the lower id first.
+// Order: logits descending, equal logits by ascending id; NaN ranks as -inf.
+// The k-th largest of the 32 lane maxima (maxima of distinct experts) is a lower bound tau
+// of the k-th largest logit, so the top k are among the experts with logit >= tau; when
+// those candidates are at most RCAND (the usual case: about 1.5 k) each one's rank among
+// them is counted directly.  Otherwise (many equal logits) the warp selects the best k
+// one after the other: each lane keeps the maximum of its experts not yet taken, the warp
+// takes the best, and only the lane that gave it away looks for its next one.
+// cand: this warp's RCAND_WARP pairs of shared memory.
 template <int NV>
 __device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src, bool global_src, int t, int lane,
-                                           int* s_idx) {
+                                           int* s_idx, float2* cand) {
   const int E = a.E, k = a.k;
   float v[NV];
+  float m = -INFINITY;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int ee = lane + 32 * i;
-    v[i] = ee < E ? (global_src ? __ldcg(src + ee) : src[ee]) : -INFINITY;
+    const float x = ee < E ? (global_src ? __ldcg(src + ee) : src[ee]) : -INFINITY;
+    v[i] = x != x ? -INFINITY : x;
+    m = fmaxf(m, v[i]);
   }
-  uint32_t taken = 0u;
-  auto lane_best = [&](float& bv, int& be) {
-    bv = -INFINITY;
-    be = 0x7fffffff;
+  // tau = the k-th largest lane maximum (lane order breaks ties: the ranks are distinct)
+  int r = 0;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int ee = lane + 32 * i;
-      const float x = v[i] != v[i] ? -INFINITY : v[i];
-      if (ee < E && !((taken >> i) & 1u) && (x > bv || (x == bv && ee < be))) { bv = x; be = ee; }
-    }
-  };
-  float lv;
-  int le;
-  lane_best(lv, le);
+  for (int j = 0; j < 32; ++j) {
+    const float o = __shfl_sync(0xffffffffu, m, j);
+    r += (o > m || (o == m && j < lane)) ? 1 : 0;
+  }
+  const float tau = __shfl_sync(0xffffffffu, m, __ffs(__ballot_sync(0xffffffffu, r == k - 1)) - 1);
+  uint32_t cm = 0u;
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    if (lane + 32 * i < E && v[i] >= tau) { cm |= 1u << i; ++c; }
+  int inc = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  const int C = __shfl_sync(0xffffffffu, inc, 31);
   int my_e = 0;
   float my_l = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bv = lv;
-    int be = le;
+  if (C <= RCAND) {
+    float2* sel = cand + RCAND;
+    int pos = inc - c;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    for (int i = 0; i < NV; ++i)
+      if ((cm >> i) & 1u) cand[pos++] = make_float2(v[i], __int_as_float(lane + 32 * i));
+    __syncwarp();
+    for (int q = lane; q < C; q += 32) {
+      const float2 me = cand[q];
+      const int mid = __float_as_int(me.y);
+      int rk = 0;
+      for (int j = 0; j < C; ++j) {
+        const float2 o = cand[j];
+        rk += (o.x > me.x || (o.x == me.x && __float_as_int(o.y) < mid)) ? 1 : 0;
+      }
+      if (rk < k) sel[rk] = me;
     }
-    if (lane == j) { my_e = be; my_l = bv; }
-    if (be == le) {   // this lane's maximum was taken (ids are distinct across lanes)
-      taken |= 1u << ((be - lane) >> 5);
-      lane_best(lv, le);
+    __syncwarp();
+    if (lane < k) {
+      my_l = sel[lane].x;
+      my_e = __float_as_int(sel[lane].y);
+    }
+    __syncwarp();   // the buffers are this warp's next token's
+  } else {
+    uint32_t taken = 0u;
+    auto lane_best = [&](float& bv, int& be) {
+      bv = -INFINITY;
+      be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int ee = lane + 32 * i;
+        if (ee < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && ee < be))) { bv = v[i]; be = ee; }
+      }
+    };
+    float lv;
+    int le;
+    lane_best(lv, le);
+    for (int j = 0; j < k; ++j) {
+      float bv = lv;
+      int be = le;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+      }
+      if (lane == j) { my_e = be; my_l = bv; }
+      if (be == le) {   // this lane's maximum was taken (ids are distinct across lanes)
+        taken |= 1u << ((be - lane) >> 5);
+        lane_best(lv, le);
+      }
     }
   }
   // weights over the k selected (rank order = lane order)
@@ -120,18 +173,22 @@ __device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src
 
 // Phase 2 of the router, in one block: top-k per token from the logits lsrc [T][E]
 // (global memory when global_src), the weights, and the bucketing of the (token, rank)
-// pairs into passes.  s_cnt must be zero and the logits complete (after a barrier).
+// pairs into passes.  s_cnt must be zero and the logits complete (after a barrier);
+// s_cand holds RCAND_WARP pairs per warp.  SMALL: E <= 128 (one top-k variant).
+template <bool SMALL>
 __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* lsrc, bool global_src, int* s_cnt,
-                                              int* s_off, int* s_idx, int* s_pos, int* s_routed) {
+                                              int* s_off, int* s_idx, int* s_pos, int* s_routed, float2* s_cand) {
+  __shared__ int s_wsum[64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int E = a.E, T = a.T, k = a.k, pmax = a.pmax;
   // ---------------- phase 2a: top-k per token (one warp per token)
+  float2* cand = s_cand + (size_t)warp * RCAND_WARP;
   for (int t = warp; t < T; t += nwarps) {
     const float* src = lsrc + (size_t)t * E;
-    if (E <= 128) topk_token<4>(a, src, global_src, t, lane, s_idx);
-    else if (E <= 256) topk_token<8>(a, src, global_src, t, lane, s_idx);
-    else if (E <= 512) topk_token<16>(a, src, global_src, t, lane, s_idx);
-    else topk_token<32>(a, src, global_src, t, lane, s_idx);
+    if (SMALL || E <= 128) topk_token<4>(a, src, global_src, t, lane, s_idx, cand);
+    else if (E <= 256) topk_token<8>(a, src, global_src, t, lane, s_idx, cand);
+    else if (E <= 512) topk_token<16>(a, src, global_src, t, lane, s_idx, cand);
+    else topk_token<32>(a, src, global_src, t, lane, s_idx, cand);
   }
   __syncthreads();
 
@@ -146,13 +203,18 @@ __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* 
       }
       __syncwarp();
     }
-    // exclusive scan over experts of (passes, unique flag); lane owns a contiguous run
-    const int run = cdiv(E, 32);
-    const int e0 = min(E, lane * run), e1 = min(E, e0 + run);
+  }
+  __syncthreads();
+  {
+    // exclusive scan over experts of (passes, unique flag): a thread owns a contiguous run
+    // of experts, warps scan with shuffles, the warp totals go through shared memory
+    const int run = cdiv(E, (int)blockDim.x);
+    const int e0 = min(E, (int)threadIdx.x * run), e1 = min(E, e0 + run);
     int np = 0, nu = 0;
     for (int ee = e0; ee < e1; ++ee) {
-      np += cdiv(s_cnt[ee], pmax);
-      nu += s_cnt[ee] > 0;
+      const int c = s_cnt[ee];
+      np += pmax == 1 ? c : cdiv(c, pmax);
+      nu += c > 0;
     }
     int inp = np, inu = nu;
 #pragma unroll
@@ -161,16 +223,19 @@ __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* 
       const int a2 = __shfl_up_sync(0xffffffffu, inu, o);
       if (lane >= o) { inp += a1; inu += a2; }
     }
-    int off = inp - np, uoff = inu - nu;
+    if (lane == 31) { s_wsum[warp] = inp; s_wsum[32 + warp] = inu; }
+    __syncthreads();
+    int bp = 0, bu = 0;
+    for (int w = 0; w < warp; ++w) { bp += s_wsum[w]; bu += s_wsum[32 + w]; }
+    int off = bp + inp - np, uoff = bu + inu - nu;
     for (int ee = e0; ee < e1; ++ee) {
       s_off[ee] = off;
       const int c = s_cnt[ee];
       if (c > 0) a.plan.uniq[uoff++] = ee;
-      off += cdiv(c, pmax);
+      off += pmax == 1 ? c : cdiv(c, pmax);
     }
-    const int tot_p = __shfl_sync(0xffffffffu, inp, 31);
-    const int tot_u = __shfl_sync(0xffffffffu, inu, 31);
-    if (lane == 0) {
+    if (threadIdx.x == blockDim.x - 1) {
+      const int tot_p = bp + inp, tot_u = bu + inu;
       const int nsh = a.has_shared ? cdiv(T, pmax) : 0;
       a.plan.hdr->n_pass = tot_p + nsh;
       a.plan.hdr->n_routed_pass = tot_p;
@@ -269,8 +334,16 @@ __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* 
   }
 }
 
-// MINB = blocks per SM the registers must allow: 3 where the grid is larger than two
-// blocks per SM (so it still runs in one wave), else 1 (no register cap).
+// 4-byte word of the dynamic shared memory where phase 2's candidate pairs start (after
+// s_cnt, s_off, s_idx and s_pos; 8-byte aligned)
+__host__ __device__ __forceinline__ size_t router_cand_word(int E, int T, int k) {
+  const size_t w = (size_t)2 * E + (size_t)2 * T * k;
+  return (w + 1) & ~(size_t)1;
+}
+
+// H > 8 slices.  MINB = blocks per SM the registers must allow: 3 where the grid is
+// larger than two blocks per SM (so it still runs in one wave), else 1 (no register cap).
+// No block of this kernel waits on another.
 template <int MINB>
 __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
   extern __shared__ __align__(16) int sm[];
@@ -373,34 +446,28 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
     }
   }
 
-  // ---------------- tickets.  Small problems: the last block overall adds the slices
-  // itself.  Otherwise the last block of each expert group adds its group's slices into
-  // the logits, and the last group continues.  Both add the slices in ascending order.
-  const bool two_level = router_two_level(NS, a.T, a.E);
-  float* logits = a.partial + (size_t)NS * a.T * a.E;   // [T][E] (two-level only)
+  // ---------------- tickets: the last block of each expert group adds its group's slices
+  // into the logits in ascending slice order, and the last group continues
+  float* logits = a.partial + (size_t)NS * a.T * a.E;   // [T][E]
   __threadfence();
   __syncthreads();
-  if (two_level) {
-    if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket + 1 + g, 1u) == (unsigned)NS - 1);
-    __syncthreads();
-    if (!s_flag) return;
-    __threadfence();
-    const int ne = min(REPB, a.E - g * REPB);
-    for (int q = threadIdx.x; q < a.T * ne; q += blockDim.x) {
-      const int t = q / ne, ee = g * REPB + q % ne;
-      const float* pp = a.partial + (size_t)t * a.E + ee;
-      float v = 0.f;
+  if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket + 1 + g, 1u) == (unsigned)NS - 1);
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+  const int ne = min(REPB, a.E - g * REPB);
+  for (int q = threadIdx.x; q < a.T * ne; q += blockDim.x) {
+    const int t = q / ne, ee = g * REPB + q % ne;
+    const float* pp = a.partial + (size_t)t * a.E + ee;
+    float v = 0.f;
 #pragma unroll 8
-      for (int ss = 0; ss < NS; ++ss) v += __ldcg(pp + (size_t)ss * a.T * a.E);
-      logits[(size_t)t * a.E + ee] = v;
-    }
-    if (threadIdx.x == 0) a.ticket[1 + g] = 0u;  // ready for the next launch (stream-ordered)
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket, 1u) == (unsigned)NG - 1);
-  } else {
-    if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket, 1u) == gridDim.x - 1);
+    for (int ss = 0; ss < NS; ++ss) v += __ldcg(pp + (size_t)ss * a.T * a.E);
+    logits[(size_t)t * a.E + ee] = v;
   }
+  if (threadIdx.x == 0) a.ticket[1 + g] = 0u;  // ready for the next launch (stream-ordered)
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket, 1u) == (unsigned)NG - 1);
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
@@ -410,35 +477,202 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
   int* s_off = s_cnt + E;           // [E]
   int* s_idx = s_off + E;           // [T*k]
   int* s_pos = s_idx + T * k;       // [T*k]
-  float* slog = reinterpret_cast<float*>(s_pos + T * k);   // [T][E] (single-level only)
+  float2* s_cand = reinterpret_cast<float2*>(sm + router_cand_word(E, T, k));
   for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
-  if (!two_level) {
-    // logits = slice partials added in ascending slice order, all (t, e) in parallel
-    const size_t TE = (size_t)T * E;
-    for (int q0 = threadIdx.x; q0 < (int)TE; q0 += 2 * blockDim.x) {
-      float p[2][RNS_ONE];
+  __syncthreads();
+
+  router_finish<false>(a, logits, true, s_cnt, s_off, s_idx, s_pos, &s_routed, s_cand);
+}
+
+
+// ---------------------------------------------------------------- clusters of slices
+// H <= RCLUSTER_MAX * RSW: the NS slice blocks of an expert group are one thread-block
+// cluster (block (s, g) is rank s) and meet in distributed shared memory instead of
+// global partials.  Fused stack step: the inverse RMS is block_inv_rms's fixed tree
+// spread over the cluster: rank s computes the tree's logical warps s, s + NS, ... (the
+// same elements in the same order) and every block adds the 8 warp sums, read from their
+// owners, in the tree's order, so the bits are those of block_inv_rms.  After the partial
+// dot products, rank s adds, for its share of the group's (token, expert) logits, the NS
+// partials in ascending slice order (as router_kernel does) and writes the logit; then
+// the cluster's first block takes the group's ticket and the last group runs phase 2.
+constexpr int RCLUSTER_MAX = 8;
+namespace cg = cooperative_groups;
+
+template <int MINB>
+__global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) int sm[];
+  constexpr int NLW = RMS_NTHR / 32;   // logical warps of the norm tree
+  __shared__ float s_inv[ROUTER_FUSED_MAXT];
+  __shared__ float s_nrm[ROUTER_FUSED_MAXT][NLW];
+  __shared__ int s_flag, s_routed;
+  cg::cluster_group cl = cg::this_cluster();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = cdiv(a.H, RSW), NG = cdiv(a.E, REPB);
+  const int sl = blockIdx.x % NS, g = blockIdx.x / NS;
+  const int h0 = sl * RSW;
+  const int e = g * REPB + warp;
+  const bool live = e < a.E;
+  const bool fused = a.xres != nullptr;
+  const int T = a.T, H = a.H;
+
+  float4 wv[RSW / 128];
+  {
+    const float* wr = a.W + (size_t)(live ? e : 0) * H;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = q0 + u * blockDim.x;
+    for (int i = 0; i < RSW / 128; ++i) {
+      const int h = h0 + 4 * (lane + 32 * i);
+      wv[i] = (live && h < H) ? __ldg(reinterpret_cast<const float4*>(wr + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  pdl_wait();  // x (and the residual) come from the kernels before
+  pdl_launch_dependents();
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);                                  // [min(T, RTG)][RSW]
+  float* s_part = reinterpret_cast<float*>(sm) + (size_t)min(T, RTG) * RSW / 2;     // [T][REPB]
+  if (fused) {
+    const int hq = 4 * threadIdx.x, h = h0 + hq;
+    const bool in = threadIdx.x < RSW / 4 && h < H;
+    float4 xv[ROUTER_FUSED_MAXT];
 #pragma unroll
-        for (int ss = 0; ss < RNS_ONE; ++ss) p[u][ss] = (ss < NS && q < (int)TE) ? __ldcg(a.partial + ss * TE + q) : 0.f;
+    for (int t = 0; t < ROUTER_FUSED_MAXT; ++t) {
+      xv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < T && in) {
+        const size_t o = (size_t)t * H + h;
+        xv[t] = __ldcg(reinterpret_cast<const float4*>(a.xres + o));
+        if (a.yprev) {
+          const float4 y4 = __ldcg(reinterpret_cast<const float4*>(a.yprev + o));
+          xv[t].x += y4.x; xv[t].y += y4.y; xv[t].z += y4.z; xv[t].w += y4.w;
+        }
+      }
+    }
+    // this rank's logical warps of every token's tree: lane = logical lane
+    const int n4 = H >> 2;
+    for (int p = warp; p < T * NLW; p += 8) {
+      const int t = p / NLW, lw = p - t * NLW;
+      if (lw % NS != sl) continue;
+      const float4* x4 = reinterpret_cast<const float4*>(a.xres + (size_t)t * H);
+      const float4* y4 = a.yprev ? reinterpret_cast<const float4*>(a.yprev + (size_t)t * H) : nullptr;
+      float ss = 0.f;
+      for (int i0 = lw * 32 + lane; i0 < n4; i0 += 8 * RMS_NTHR) {
+        float4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = i0 + q * RMS_NTHR;
+          v[q] = i < n4 ? __ldcg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (y4 && i < n4) {
+            const float4 b = __ldcg(y4 + i);
+            v[q].x += b.x; v[q].y += b.y; v[q].z += b.z; v[q].w += b.w;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          ss = fmaf(v[q].x, v[q].x, ss);
+          ss = fmaf(v[q].y, v[q].y, ss);
+          ss = fmaf(v[q].z, v[q].z, ss);
+          ss = fmaf(v[q].w, v[q].w, ss);
+        }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = q0 + u * blockDim.x;
-        float v = 0.f;
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s_nrm[t][lw] = ss;
+    }
+    cl.sync();   // every rank's warp sums are written
+    if (warp < T) {
+      float v = 0.f;
+      if (lane < NLW) v = *cl.map_shared_rank(&s_nrm[warp][lane], (unsigned)(lane % NS));
 #pragma unroll
-        for (int ss = 0; ss < RNS_ONE; ++ss)
-          if (ss < NS) v += p[u][ss];
-        if (q < (int)TE) slog[q] = v;
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) s_inv[warp] = rsqrtf(v / (float)H + a.eps);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < ROUTER_FUSED_MAXT; ++t) {
+      if (t < T && threadIdx.x < RSW / 4) {
+        const float inv = s_inv[t];
+        uint2 v;
+        v.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].x * inv)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].y * inv)) << 16);
+        v.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].z * inv)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].w * inv)) << 16);
+        if (!in) v = make_uint2(0u, 0u);
+        *reinterpret_cast<uint2*>(xs + t * RSW + hq) = v;
+        if (g == 0 && in) *reinterpret_cast<uint2*>(a.xn_out + (size_t)t * H + h) = v;
       }
     }
   }
-  __syncthreads();
 
-  router_finish(a, two_level ? logits : slog, two_level, s_cnt, s_off, s_idx, s_pos, &s_routed);
+  // ---------------- phase 1: partial logits of slice sl into s_part [T][REPB]
+  for (int tg = 0; tg < T; tg += RTG) {
+    const int nt = min(RTG, T - tg);
+    __syncthreads();  // the previous group's reads of xs are done (fused: xs is staged)
+    if (!fused) {
+      for (int q = threadIdx.x; q < nt * (RSW / 4); q += blockDim.x) {
+        const int tl = q / (RSW / 4), hq = 4 * (q % (RSW / 4)), h = h0 + hq;
+        uint2 v = make_uint2(0u, 0u);
+        if (h < H) v = __ldg(reinterpret_cast<const uint2*>(a.x + (size_t)(tg + tl) * H + h));
+        *reinterpret_cast<uint2*>(xs + tl * RSW + hq) = v;
+      }
+      __syncthreads();
+    }
+    if (live) {
+      float keep = 0.f;
+      for (int tl = 0; tl < nt; ++tl) {
+        const uint16_t* xr = xs + tl * RSW;
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < RSW / 128; ++i) {
+          const uint2 xb = *reinterpret_cast<const uint2*>(xr + 4 * (lane + 32 * i));
+          acc = fmaf(wv[i].x, __uint_as_float(xb.x << 16), acc);
+          acc = fmaf(wv[i].y, __uint_as_float(xb.x & 0xffff0000u), acc);
+          acc = fmaf(wv[i].z, __uint_as_float(xb.y << 16), acc);
+          acc = fmaf(wv[i].w, __uint_as_float(xb.y & 0xffff0000u), acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == tl) keep = acc;
+      }
+      if (lane < nt) s_part[(tg + lane) * REPB + warp] = keep;
+    }
+  }
+
+  // ---------------- the group's logits: rank sl adds items q = sl, sl + NS, ...
+  cl.sync();   // every rank's partials are written
+  float* logits = a.partial + (size_t)NS * T * a.E;   // [T][E]
+  const int ne = min(REPB, a.E - g * REPB);
+  for (int q = sl + NS * (int)threadIdx.x; q < T * REPB; q += NS * (int)blockDim.x) {
+    const int t = q / REPB, w = q - t * REPB;
+    if (w < ne) {
+      float v = 0.f;
+      for (int r = 0; r < NS; ++r) v += cl.map_shared_rank(s_part, (unsigned)r)[q];
+      logits[(size_t)t * a.E + g * REPB + w] = v;
+    }
+  }
+  __threadfence();
+  cl.sync();   // no rank reads another's shared memory after this; the group's logits are written
+  if (sl != 0) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_flag = (atomicAdd(a.ticket, 1u) == (unsigned)NG - 1);
+  }
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+
+  const int E = a.E, k = a.k;
+  int* s_cnt = sm;                  // [E]
+  int* s_off = s_cnt + E;           // [E]
+  int* s_idx = s_off + E;           // [T*k]
+  int* s_pos = s_idx + T * k;       // [T*k]
+  float2* s_cand = reinterpret_cast<float2*>(sm + router_cand_word(E, T, k));
+  for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
+  __syncthreads();
+  router_finish<false>(a, logits, true, s_cnt, s_off, s_idx, s_pos, &s_routed, s_cand);
 }
 
+size_t router_cluster_smem(int H, int T, int E, int k) {
+  const size_t p1 = (size_t)std::min(T, RTG) * RSW * 2 + (size_t)T * REPB * sizeof(float);
+  const size_t p2 = router_cand_word(E, T, k) * 4 + (size_t)(256 / 32) * RCAND_WARP * sizeof(float2);
+  return std::max(p1, p2);
+}
 
 // ---------------------------------------------------------------- small problems, one block
 // When every (expert, slice) item fits one warp of a single 1024-thread block and the
@@ -447,12 +681,17 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
 // W slice before the wait; logits are the slices added in ascending order, as in
 // router_kernel, so both give the same bits.
 constexpr int RSMALL_THREADS = 1024;
+constexpr int ROUTER_SMEM_MAX = 160 * 1024;
 __host__ __device__ __forceinline__ bool router_small_fits(int H, int T, int E) {
   return E * cdiv(H, RSW) <= RSMALL_THREADS / 32 && T * H <= 32768 && T <= 32;
 }
+// 4-byte word where router_small_kernel's candidate pairs start (8-byte aligned)
+__host__ __device__ __forceinline__ size_t router_small_cand_word(int H, int T, int E, int k) {
+  const size_t w = (size_t)T * H / 2 + (size_t)T * E * cdiv(H, RSW) + (size_t)T * E + (size_t)2 * E + (size_t)2 * T * k;
+  return (w + 1) & ~(size_t)1;
+}
 size_t router_small_smem(int H, int T, int E, int k) {
-  return (size_t)T * H * 2 + (size_t)T * E * cdiv(H, RSW) * 4 + (size_t)T * E * 4 +
-         (size_t)(2 * E + 2 * T * k) * sizeof(int);
+  return router_small_cand_word(H, T, E, k) * 4 + (size_t)(RSMALL_THREADS / 32) * RCAND_WARP * sizeof(float2);
 }
 
 // V4: float4s of a row each norm thread holds in registers (H <= 4 * RMS_NTHR * V4)
@@ -581,33 +820,48 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
     slog[q] = v;
   }
   __syncthreads();
-  router_finish(a, slog, false, s_cnt, s_off, s_idx, s_pos, &s_routed);
+  router_finish<true>(a, slog, false, s_cnt, s_off, s_idx, s_pos, &s_routed,
+                reinterpret_cast<float2*>(sm + router_small_cand_word(H, T, E, k)));
 }
 
 cudaError_t router_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  cudaError_t e = cudaFuncSetAttribute(router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, ROUTER_SMEM_MAX);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(router_small_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  e = cudaFuncSetAttribute(router_small_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, ROUTER_SMEM_MAX);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(router_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  e = cudaFuncSetAttribute(router_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, ROUTER_SMEM_MAX);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(router_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  e = cudaFuncSetAttribute(router_cluster_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, ROUTER_SMEM_MAX);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_cluster_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, ROUTER_SMEM_MAX);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(router_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, ROUTER_SMEM_MAX);
 }
 
+// staging of min(T, RTG) bf16 rows of a slice, then (last block) the phase-2 arrays
 size_t router_smem_bytes(int H, int T, int E, int k) {
-  const size_t p2 = (size_t)(2 * E + 2 * T * k) * sizeof(int) +
-                    (router_two_level(cdiv(H, RSW), T, E) ? 0 : (size_t)T * E * sizeof(float));
-  return std::max((size_t)RXS_BYTES, p2);
+  (void)H;
+  const size_t p2 = router_cand_word(E, T, k) * 4 + (size_t)(256 / 32) * RCAND_WARP * sizeof(float2);
+  return std::max((size_t)std::min(T, RTG) * RSW * 2, p2);
 }
 
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s) {
   if (router_small_fits(a.H, a.T, a.E)) {
     const size_t smem = router_small_smem(a.H, a.T, a.E, a.k);
+    if (smem > ROUTER_SMEM_MAX) return cudaErrorInvalidValue;
     if (a.H <= 4 * RMS_NTHR * 4) return launch_pdl(router_small_kernel<4>, 1, RSMALL_THREADS, smem, s, a);
     return launch_pdl(router_small_kernel<8>, 1, RSMALL_THREADS, smem, s, a);
   }
-  const int grid = cdiv(a.H, RSW) * cdiv(a.E, REPB);
+  const int NS = cdiv(a.H, RSW);
+  const int grid = NS * cdiv(a.E, REPB);
+  if (NS <= RCLUSTER_MAX) {
+    const size_t smem = router_cluster_smem(a.H, a.T, a.E, a.k);
+    if (smem > ROUTER_SMEM_MAX) return cudaErrorInvalidValue;
+    if (grid > 2 * num_sms) return launch_pdl_cluster(router_cluster_kernel<3>, grid, 256, NS, smem, s, a);
+    return launch_pdl_cluster(router_cluster_kernel<1>, grid, 256, NS, smem, s, a);
+  }
   const size_t smem = router_smem_bytes(a.H, a.T, a.E, a.k);
+  if (smem > ROUTER_SMEM_MAX) return cudaErrorInvalidValue;
   if (grid > 2 * num_sms) return launch_pdl(router_kernel<3>, grid, 256, smem, s, a);
   return launch_pdl(router_kernel<1>, grid, 256, smem, s, a);
 }

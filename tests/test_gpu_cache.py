@@ -167,20 +167,23 @@ def test_bounded_device_wait_reports_timeout():
     ctx.close()
 
 
-# wide rows: the single-block router (8 experts x 4 slices) and the multi-block one (16 x 7)
+# wide rows: the single-block router (8 experts x 4 slices), the cluster router (16
+# experts x 7 slices, a cluster per expert group) and the one for more than 8 slices
 SPEC_H4K = LayerSpec(4096, 256, 8, 2, S.INT4, router=0, seed=23, layers=2)
 SPEC_H7K = LayerSpec(7168, 256, 16, 4, S.RVQ, router=0, seed=24, layers=2)
+SPEC_H9K = LayerSpec(8448, 128, 24, 4, S.RVQ, router=1, seed=25, layers=2)
 
 
-@pytest.mark.parametrize("spec", [SPEC, SPEC4, SPEC_H4K, SPEC_H7K])
-def test_fused_stack_step_equals_separate_calls(spec):
+@pytest.mark.parametrize("spec,T", [(SPEC, 1), (SPEC4, 1), (SPEC_H4K, 1), (SPEC_H7K, 1), (SPEC_H7K, 4),
+                                    (SPEC_H9K, 1), (SPEC_H9K, 3)])
+def test_fused_stack_step_equals_separate_calls(spec, T):
     """moe_forward_residual == moe_residual_rmsnorm + moe_forward, bit for bit."""
     import torch
-    ctx = make_context(spec, 1)
-    seq = _tokens(spec, 5)
+    ctx = make_context(spec, T)
+    seq = _tokens(spec, 5, T)
     ref, _ = _stack_run(ctx, spec, seq)
     outs = []
-    T, H = 1, spec.H
+    H = spec.H
     x = torch.zeros((T, H), dtype=torch.float32, device="cuda")
     y = torch.zeros_like(x)
     xn = torch.zeros((T, H), dtype=torch.int16, device="cuda")

@@ -45,7 +45,10 @@ def test_tiny_config_rvq_top2_softmax():
     (512, 384, 4, 2, 16, 1, True),      # T = 16: most experts take the dense path
     (264, 200, 3, 3, 40, 0, False),     # 40 tokens on every expert: split into 2 dense groups
     (64, 48, 1, 1, 5, 1, False),        # a single expert, k = 1 (weight 1 for both score kinds)
-    (128, 96, 12, 3, 256, 0, True),     # the largest T (256): many dense groups, the two-level router
+    (128, 96, 12, 3, 256, 0, True),     # the largest T (256): many dense groups
+    (2048, 64, 40, 4, 5, 0, True),      # router clusters of 2 slices
+    (2560, 128, 24, 3, 40, 1, False),   # clusters of 3 (a ragged slice), two 32-token staging groups
+    (8448, 64, 40, 4, 3, 1, False),     # 9 slices: the router without clusters
 ])
 def test_rvq_odd_shapes(H, F, E, k, T, router, shared):
     _run(LayerSpec(H, F, E, k, S.RVQ, router=router, shared=shared, seed=H + F + E), T)
@@ -59,6 +62,7 @@ def test_rvq_odd_shapes(H, F, E, k, T, router, shared):
     (256, 128, 8, 2, 32, 1, True),      # T = 32: experts with > 4 tokens take several passes
     (128, 128, 1, 1, 3, 0, False),      # a single expert, k = 1
     (256, 256, 12, 3, 256, 1, True),    # the largest T (256): up to 4 tokens per pass, many passes
+    (2304, 256, 20, 2, 3, 0, False),    # router clusters of 3 slices, the last ragged
 ])
 def test_int4_odd_shapes(H, F, E, k, T, router, shared):
     _run(LayerSpec(H, F, E, k, S.INT4, router=router, shared=shared, seed=H + F + E), T)

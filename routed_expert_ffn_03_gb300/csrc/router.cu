@@ -109,6 +109,7 @@ __device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src
       const float2 me = cand[q];
       const int mid = __float_as_int(me.y);
       int rk = 0;
+#pragma unroll 8
       for (int j = 0; j < C; ++j) {
         const float2 o = cand[j];
         rk += (o.x > me.x || (o.x == me.x && __float_as_int(o.y) < mid)) ? 1 : 0;
@@ -181,8 +182,56 @@ __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* 
   __shared__ int s_wsum[64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int E = a.E, T = a.T, k = a.k, pmax = a.pmax;
-  // ---------------- phase 2a: top-k per token (one warp per token)
   float2* cand = s_cand + (size_t)warp * RCAND_WARP;
+  if (T == 1 && a.big_min != 1) {
+    // one token, in warp 0 alone: every selected expert has one pass, the passes in
+    // ascending expert id, the shared expert's last; no expert reaches a dense group
+    if (warp != 0) return;
+    if (SMALL || E <= 128) topk_token<4>(a, lsrc, global_src, 0, lane, s_idx, cand);
+    else if (E <= 256) topk_token<8>(a, lsrc, global_src, 0, lane, s_idx, cand);
+    else if (E <= 512) topk_token<16>(a, lsrc, global_src, 0, lane, s_idx, cand);
+    else topk_token<32>(a, lsrc, global_src, 0, lane, s_idx, cand);
+    __syncwarp();
+    const int ee = lane < k ? s_idx[lane] : 0x7fffffff;
+    int p = 0;   // rank of the expert among the k by id (the k ids are distinct)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) p += __shfl_sync(0xffffffffu, ee, j) < ee ? 1 : 0;
+    if (lane < k) {
+      a.plan.uniq[p] = ee;
+      a.plan.pass_expert[p] = ee;
+      a.plan.pass_ntok[p] = 1;
+      a.plan.pass_tok[p * pmax] = 0;
+      a.plan.pair_pass[lane] = p;
+      a.plan.pair_slot[lane] = 0;
+    }
+    const int n_pass = k + (a.has_shared ? 1 : 0);
+    if (a.big_min > 0)
+      for (int q = lane; q < n_pass; q += 32) a.plan.small_order[q] = q;
+    if (lane == 0) {
+      if (a.has_shared) {
+        a.plan.pass_tok[k * pmax] = 0;
+        a.plan.shared_pass[0] = k;
+        a.plan.shared_slot[0] = 0;
+        a.plan.pass_expert[k] = E;
+        a.plan.pass_ntok[k] = 1;
+      }
+      a.plan.hdr->n_pass = n_pass;
+      a.plan.hdr->n_routed_pass = k;
+      a.plan.hdr->n_uniq = k;
+      a.plan.hdr->T = 1;
+      a.plan.hdr->n_big = 0;
+      a.plan.hdr->n_small = n_pass;
+      DevCounters* dc = a.counters;
+      atomicAdd(&dc->forwards, 1ull);
+      atomicAdd(&dc->tokens, 1ull);
+      atomicAdd(&dc->lookups, (unsigned long long)k);
+      atomicAdd(&dc->bytes_touched, (unsigned long long)n_pass * a.record_bytes);
+      atomicAdd(&dc->bytes_router, (unsigned long long)E * a.H * 4ull);
+      *a.ticket = 0u;  // ready for the next launch (stream-ordered)
+    }
+    return;
+  }
+  // ---------------- phase 2a: top-k per token (one warp per token)
   for (int t = warp; t < T; t += nwarps) {
     const float* src = lsrc + (size_t)t * E;
     if (SMALL || E <= 128) topk_token<4>(a, src, global_src, t, lane, s_idx, cand);
@@ -488,13 +537,17 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
 // ---------------------------------------------------------------- clusters of slices
 // H <= RCLUSTER_MAX * RSW: the NS slice blocks of an expert group are one thread-block
 // cluster (block (s, g) is rank s) and meet in distributed shared memory instead of
-// global partials.  Fused stack step: the inverse RMS is block_inv_rms's fixed tree
-// spread over the cluster: rank s computes the tree's logical warps s, s + NS, ... (the
-// same elements in the same order) and every block adds the 8 warp sums, read from their
-// owners, in the tree's order, so the bits are those of block_inv_rms.  After the partial
-// dot products, rank s adds, for its share of the group's (token, expert) logits, the NS
-// partials in ascending slice order (as router_kernel does) and writes the logit; then
-// the cluster's first block takes the group's ticket and the last group runs phase 2.
+// global partials.  Values are pushed: a rank stores into the others' shared memory and
+// one cluster barrier later every reader finds them in its own.  Fused stack step: the
+// inverse RMS is block_inv_rms's fixed tree spread over the cluster: rank s computes the
+// tree's logical warps s, s + NS, ... (the same elements in the same order) and stores
+// the warp sums in every rank; each block then adds the 8 warp sums in the tree's order,
+// so the bits are those of block_inv_rms.  The partial dot products go to rank 0, which
+// adds the NS partials of each (token, expert) in ascending slice order (as router_kernel
+// does), writes the group's logits and takes the group's ticket; the other ranks are done
+// after the barrier, and the last group runs phase 2.  A first barrier phase, arrived at
+// on entry and waited for before the first remote store, makes sure that every block of
+// the cluster has started.
 constexpr int RCLUSTER_MAX = 8;
 namespace cg = cooperative_groups;
 
@@ -506,6 +559,7 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
   __shared__ float s_nrm[ROUTER_FUSED_MAXT][NLW];
   __shared__ int s_flag, s_routed;
   cg::cluster_group cl = cg::this_cluster();
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");   // this block has started
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = cdiv(a.H, RSW), NG = cdiv(a.E, REPB);
   const int sl = blockIdx.x % NS, g = blockIdx.x / NS;
@@ -528,7 +582,8 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
   pdl_wait();  // x (and the residual) come from the kernels before
   pdl_launch_dependents();
   uint16_t* xs = reinterpret_cast<uint16_t*>(sm);                                  // [min(T, RTG)][RSW]
-  float* s_part = reinterpret_cast<float*>(sm) + (size_t)min(T, RTG) * RSW / 2;     // [T][REPB]
+  float* s_part = reinterpret_cast<float*>(sm) + (size_t)min(T, RTG) * RSW / 2;     // [NS][T][REPB] (rank 0)
+  bool started = false;   // the entry barrier phase has been waited for
   if (fused) {
     const int hq = 4 * threadIdx.x, h = h0 + hq;
     const bool in = threadIdx.x < RSW / 4 && h < H;
@@ -547,6 +602,8 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
     }
     // this rank's logical warps of every token's tree: lane = logical lane
     const int n4 = H >> 2;
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every block has started
+    started = true;
     for (int p = warp; p < T * NLW; p += 8) {
       const int t = p / NLW, lw = p - t * NLW;
       if (lw % NS != sl) continue;
@@ -574,12 +631,12 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) s_nrm[t][lw] = ss;
+      if (lane < NS) *cl.map_shared_rank(&s_nrm[t][lw], (unsigned)lane) = ss;   // (every lane holds the sum)
     }
-    cl.sync();   // every rank's warp sums are written
+    cl.sync();   // every rank's warp sums are in every rank
     if (warp < T) {
       float v = 0.f;
-      if (lane < NLW) v = *cl.map_shared_rank(&s_nrm[warp][lane], (unsigned)(lane % NS));
+      if (lane < NLW) v = s_nrm[warp][lane];
 #pragma unroll
       for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0) s_inv[warp] = rsqrtf(v / (float)H + a.eps);
@@ -601,7 +658,9 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
     }
   }
 
-  // ---------------- phase 1: partial logits of slice sl into s_part [T][REPB]
+  // ---------------- phase 1: partial logits of slice sl into rank 0's s_part [sl][T][REPB]
+  if (!started) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every block has started
+  float* part0 = cl.map_shared_rank(s_part, 0u) + (size_t)sl * T * REPB;
   for (int tg = 0; tg < T; tg += RTG) {
     const int nt = min(RTG, T - tg);
     __syncthreads();  // the previous group's reads of xs are done (fused: xs is staged)
@@ -630,25 +689,24 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
         acc = warp_sum(acc);
         if (lane == tl) keep = acc;
       }
-      if (lane < nt) s_part[(tg + lane) * REPB + warp] = keep;
+      if (lane < nt) part0[(tg + lane) * REPB + warp] = keep;
     }
   }
 
-  // ---------------- the group's logits: rank sl adds items q = sl, sl + NS, ...
-  cl.sync();   // every rank's partials are written
+  // ---------------- the group's logits, in rank 0
+  cl.sync();   // every rank's partials are in rank 0
+  if (sl != 0) return;
   float* logits = a.partial + (size_t)NS * T * a.E;   // [T][E]
   const int ne = min(REPB, a.E - g * REPB);
-  for (int q = sl + NS * (int)threadIdx.x; q < T * REPB; q += NS * (int)blockDim.x) {
+  for (int q = threadIdx.x; q < T * REPB; q += blockDim.x) {
     const int t = q / REPB, w = q - t * REPB;
     if (w < ne) {
       float v = 0.f;
-      for (int r = 0; r < NS; ++r) v += cl.map_shared_rank(s_part, (unsigned)r)[q];
+      for (int r = 0; r < NS; ++r) v += s_part[((size_t)r * T + t) * REPB + w];
       logits[(size_t)t * a.E + g * REPB + w] = v;
     }
   }
-  __threadfence();
-  cl.sync();   // no rank reads another's shared memory after this; the group's logits are written
-  if (sl != 0) return;
+  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     s_flag = (atomicAdd(a.ticket, 1u) == (unsigned)NG - 1);
@@ -669,7 +727,7 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
 }
 
 size_t router_cluster_smem(int H, int T, int E, int k) {
-  const size_t p1 = (size_t)std::min(T, RTG) * RSW * 2 + (size_t)T * REPB * sizeof(float);
+  const size_t p1 = (size_t)std::min(T, RTG) * RSW * 2 + (size_t)cdiv(H, RSW) * T * REPB * sizeof(float);
   const size_t p2 = router_cand_word(E, T, k) * 4 + (size_t)(256 / 32) * RCAND_WARP * sizeof(float2);
   return std::max(p1, p2);
 }

@@ -79,6 +79,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 // Start moving `bytes` (a multiple of 16, 16-B aligned) from global memory into L2 so a
 // later load hits there; no completion to wait for.
+// atomic add with acquire-release semantics at GPU scope: the writes this thread has
+// seen (its block's, after a barrier) are visible to whoever reads the new value, and
+// what that thread wrote before is visible here
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }

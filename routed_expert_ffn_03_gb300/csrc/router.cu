@@ -706,14 +706,12 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
       logits[(size_t)t * a.E + g * REPB + w] = v;
     }
   }
+  // the group's ticket: its release publishes the logits (written before the barrier),
+  // and the last group's acquire makes every group's logits visible to this block
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_flag = (atomicAdd(a.ticket, 1u) == (unsigned)NG - 1);
-  }
+  if (threadIdx.x == 0) s_flag = (atom_add_acq_rel_gpu(a.ticket, 1u) == (unsigned)NG - 1);
   __syncthreads();
   if (!s_flag) return;
-  __threadfence();
 
   const int E = a.E, k = a.k;
   int* s_cnt = sm;                  // [E]
@@ -721,8 +719,10 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
   int* s_idx = s_off + E;           // [T*k]
   int* s_pos = s_idx + T * k;       // [T*k]
   float2* s_cand = reinterpret_cast<float2*>(sm + router_cand_word(E, T, k));
-  for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
-  __syncthreads();
+  if (T != 1 || a.big_min == 1) {   // the per-expert counts (not used by the one-token plan)
+    for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
+    __syncthreads();
+  }
   router_finish<false>(a, logits, true, s_cnt, s_off, s_idx, s_pos, &s_routed, s_cand);
 }
 

@@ -76,34 +76,44 @@ __device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src
     v[i] = x != x ? -INFINITY : x;
     m = fmaxf(m, v[i]);
   }
-  // tau = the k-th largest lane maximum (lane order breaks ties: the ranks are distinct)
-  int r = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float o = __shfl_sync(0xffffffffu, m, j);
-    r += (o > m || (o == m && j < lane)) ? 1 : 0;
-  }
-  const float tau = __shfl_sync(0xffffffffu, m, __ffs(__ballot_sync(0xffffffffu, r == k - 1)) - 1);
+  // With E <= RCAND every expert is a candidate, in place (candidate e = expert e).
+  // Otherwise tau = the k-th largest lane maximum (lane order breaks ties: the ranks are
+  // distinct), and the candidates are packed by a warp scan.
+  int C = E, inc = 0, c = 0;
   uint32_t cm = 0u;
-  int c = 0;
+  if (E > RCAND) {
+    int r = 0;
 #pragma unroll
-  for (int i = 0; i < NV; ++i)
-    if (lane + 32 * i < E && v[i] >= tau) { cm |= 1u << i; ++c; }
-  int inc = c;
+    for (int j = 0; j < 32; ++j) {
+      const float o = __shfl_sync(0xffffffffu, m, j);
+      r += (o > m || (o == m && j < lane)) ? 1 : 0;
+    }
+    const float tau = __shfl_sync(0xffffffffu, m, __ffs(__ballot_sync(0xffffffffu, r == k - 1)) - 1);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
+    for (int i = 0; i < NV; ++i)
+      if (lane + 32 * i < E && v[i] >= tau) { cm |= 1u << i; ++c; }
+    inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    C = __shfl_sync(0xffffffffu, inc, 31);
   }
-  const int C = __shfl_sync(0xffffffffu, inc, 31);
   int my_e = 0;
   float my_l = 0.f;
   if (C <= RCAND) {
     float2* sel = cand + RCAND;
-    int pos = inc - c;
+    if (E <= RCAND) {
 #pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if ((cm >> i) & 1u) cand[pos++] = make_float2(v[i], __int_as_float(lane + 32 * i));
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i < E) cand[lane + 32 * i] = make_float2(v[i], __int_as_float(lane + 32 * i));
+    } else {
+      int pos = inc - c;
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if ((cm >> i) & 1u) cand[pos++] = make_float2(v[i], __int_as_float(lane + 32 * i));
+    }
     __syncwarp();
     for (int q = lane; q < C; q += 32) {
       const float2 me = cand[q];
@@ -194,8 +204,7 @@ __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* 
     __syncwarp();
     const int ee = lane < k ? s_idx[lane] : 0x7fffffff;
     int p = 0;   // rank of the expert among the k by id (the k ids are distinct)
-#pragma unroll
-    for (int j = 0; j < 32; ++j) p += __shfl_sync(0xffffffffu, ee, j) < ee ? 1 : 0;
+    for (int j = 0; j < k; ++j) p += __shfl_sync(0xffffffffu, ee, j) < ee ? 1 : 0;
     if (lane < k) {
       a.plan.uniq[p] = ee;
       a.plan.pass_expert[p] = ee;

@@ -61,6 +61,11 @@ CONFIGS = {
                             "host pool, 32 GB HBM LRU cache, side-stream miss copies, 4096-token domain-local trace",
                    layers=48, H=7168, F=1536, E=256, k=16, router=0, shared=False, wfmt=S.RVQ, T=1,
                    tokens=4096, trace="domain", cache=32_000_000_000),
+    "stream-file": dict(workload="File tier: 16 MoE layers x 256 experts, H=7168, F=1536, top-16, RVQ-3bit, experts "
+                                 "in a local file behind a 16 GB pinned RAM LRU cache behind an 8 GB HBM LRU cache, "
+                                 "512-token domain-local trace",
+                        layers=16, H=7168, F=1536, E=256, k=16, router=0, shared=False, wfmt=S.RVQ, T=1,
+                        tokens=512, trace="domain", cache=8_000_000_000, host_cache=16_000_000_000),
 }
 # one-layer cuts of the big shapes (a few GB on the device), for profiler captures
 for _n, _src in (("mixtral1", "mixtral"), ("dsv3-1", "dsv3"), ("wide1", "wide")):
@@ -158,7 +163,8 @@ def build_context(cfg, device, max_tokens):
     t0 = time.time()
     ctx = M.Context(cfg["layers"], cfg["H"], cfg["F"], cfg["E"], cfg["k"], cfg["wfmt"], router=cfg["router"],
                     shared_ffn=cfg["F"] if cfg["shared"] else 0, max_tokens=max_tokens,
-                    hbm_cache_bytes=cfg["cache"], device=device)
+                    hbm_cache_bytes=cfg["cache"], device=device, pool_file=cfg.get("pool_file"),
+                    host_cache_bytes=int(cfg.get("host_cache", 0)))
     nb = S.expert_blob_bytes(cfg["wfmt"], cfg["H"], cfg["F"])
     blob = torch.empty(nb, dtype=torch.uint8, device="cuda:%d" % device)
     experts = list(range(cfg["E"])) + ([-1] if cfg["shared"] else [])
@@ -501,6 +507,17 @@ def run_gpu(args, cfg, rank, world, device):
                             "expert bytes copied (misses and read-ahead) / time the link was busy (union of the "
                             "copy batches)",
             "cache_slots": st["cache_slots"]}
+        if cfg.get("pool_file"):
+            out["streaming"]["file_tier"] = {
+                "file_bytes": cfg["file_bytes"], "ram_cache_bytes": int(cfg["host_cache"]),
+                "o_direct": bool(st["file_direct"]), "file_reads": st["file_reads"],
+                "ram_hits": st["ram_hits"], "ram_misses": st["ram_misses"],
+                "file_read_gbs": round(st["file_read_bytes"] / (st["file_read_ms"] / 1e3) / 1e9, 2)
+                if st["file_read_ms"] else None,
+                "file_read_ms": round(st["file_read_ms"], 2),
+                "file_read_frac_of_run": round(st["file_read_ms"] / ms, 4),
+                "read_measure": "records read from the file (4096-byte aligned, 8 reader threads) / wall time of "
+                                "the read batches, which the forward waits for"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ctx.close()
         torch.cuda.empty_cache()
@@ -588,6 +605,8 @@ def main():
     ap.add_argument("--prof-steps", type=int, default=16, help="replays of the per-kernel event graph")
     ap.add_argument("--readahead", type=int, default=1, choices=[0, 1],
                     help="streamed configs: predict the next layer's experts and copy them early")
+    ap.add_argument("--pool-file", default=None,
+                    help="stream-file: where the expert file goes (default: the temp directory)")
     ap.add_argument("--hit-sweep", type=int, default=0, metavar="TOKENS",
                     help="streamed configs: after the timed run, the LRU hit rate vs cache budget over a "
                          "routing trace of this many tokens")
@@ -599,6 +618,23 @@ def main():
     if args.tokens_per_step:
         cfg["T"] = args.tokens_per_step
         cfg["workload"] += " (T=%d per step)" % cfg["T"]
+    if cfg.get("host_cache"):
+        # the file tier: the expert file goes to --pool-file's directory (default: the temp
+        # directory); fewer layers when that filesystem lacks room for all of them
+        import tempfile
+        path = args.pool_file or os.path.join(tempfile.gettempdir(), "moe-experts-%d.bin" % os.getpid())
+        stride = (S.expert_blob_bytes(cfg["wfmt"], cfg["H"], cfg["F"]) + 4095) // 4096 * 4096
+        vfs = os.statvfs(os.path.dirname(os.path.abspath(path)))
+        free_b = vfs.f_bavail * vfs.f_frsize
+        per_layer = cfg["E"] * stride
+        fit = int((free_b * 0.8) // per_layer)
+        if fit < 2:
+            raise SystemExit("not enough room for the expert file in %s (%.1f GB free)" % (path, free_b / 1e9))
+        if fit < cfg["layers"]:
+            cfg["workload"] += " (%d of %d layers: %.0f GB free for the file)" % (fit, cfg["layers"], free_b / 1e9)
+            cfg["layers"] = fit
+        cfg["pool_file"] = path
+        cfg["file_bytes"] = cfg["layers"] * per_layer
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -71,7 +71,8 @@ typedef enum {
     MOE_ECUDA = 4,      /* a CUDA call failed (sticky) */
     MOE_ESTATE = 5,     /* a router or expert of the layer is not registered yet */
     MOE_ETIMEOUT = 6,   /* a bounded device wait ran out (sticky) */
-    MOE_ENOTFOUND = 7   /* nothing recorded yet (moe_get_routing before a forward) */
+    MOE_ENOTFOUND = 7,  /* nothing recorded yet (moe_get_routing before a forward) */
+    MOE_EIO = 8         /* the expert file could not be created, written or read */
 } moe_status;
 
 typedef enum {
@@ -96,6 +97,12 @@ typedef struct {
     int max_tokens;     /* largest T of a forward, 1..256 */
     unsigned long long hbm_cache_bytes; /* 0 = every expert resident in HBM; else the
                                            HBM budget of the expert cache in bytes */
+    const char* pool_file;              /* streamed mode: NULL = the host pool holds every
+                                           expert in pinned RAM; else the experts live in this
+                                           file (created, truncated, removed by moe_destroy)
+                                           behind a pinned RAM cache of host_cache_bytes */
+    unsigned long long host_cache_bytes; /* with pool_file: the RAM cache budget in bytes
+                                            (at least 2 k records of 4096-byte aligned size) */
 } moe_config;
 
 typedef struct {
@@ -117,16 +124,24 @@ typedef struct {
     unsigned long long prefetches;            /* records copied by read-ahead (streamed) */
     unsigned long long prefetch_hits;         /* lookups that found a record read-ahead put there
                                                  and no lookup had used yet */
+    unsigned long long file_reads;            /* records read from the expert file (pool_file) */
+    unsigned long long file_read_bytes;       /* bytes of those reads (4096-byte aligned records) */
+    unsigned long long ram_hits;              /* HBM misses served from the RAM cache (pool_file) */
+    unsigned long long ram_misses;            /* HBM misses read from the file first (pool_file) */
+    double file_read_ms;                      /* wall time of the file read batches */
+    int file_direct;                          /* 1 when the file is read with O_DIRECT */
 } moe_stats_t;
 
 typedef struct moe_ctx moe_ctx;
 
 /* Create a context on CUDA device `device`.  Allocates the HBM expert storage (all
  * experts when hbm_cache_bytes == 0, else floor(hbm_cache_bytes / record) slots),
- * the pinned host pool (streamed mode only), router storage and scratch.
- * Errors: MOE_EINVAL (bad config), MOE_EBUDGET (cache below 2 k records, or above what
- * the pool needs is allowed and clipped), MOE_ENOMEM (HBM or host memory short; checked
- * against cudaMemGetInfo before allocating), MOE_ECUDA. */
+ * the pinned host pool (streamed mode only: every expert, or with pool_file the RAM
+ * cache in front of the expert file), router storage and scratch.
+ * Errors: MOE_EINVAL (bad config; pool_file without hbm_cache_bytes), MOE_EBUDGET (HBM
+ * cache below 2 k records, or above what the pool needs is allowed and clipped; RAM cache
+ * below 2 k records), MOE_ENOMEM (HBM or host memory short; checked against
+ * cudaMemGetInfo before allocating), MOE_EIO (the expert file), MOE_ECUDA. */
 moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out);
 
 /* Register the router of `layer`: fp32 [E][H] row-major.  `w` may be host memory or
@@ -136,8 +151,9 @@ moe_status moe_register_router(moe_ctx* ctx, int layer, const float* w);
 /* Register expert `expert` (0..E-1, or -1 for the shared expert) of `layer` from its
  * boundary blob (format above).  `blob` may be host memory or device memory of the
  * context's device; `bytes` must equal moe_expert_blob_bytes().  The blob is repacked
- * into the kernel layout: into its HBM slot (resident mode) or into the pinned host
- * pool (streamed mode).  Synchronous: the blob may be freed on return. */
+ * into the kernel layout: into its HBM slot (resident mode), into the pinned host pool
+ * (streamed mode) or into the expert file (pool_file).  Synchronous: the blob may be freed
+ * on return.  MOE_EIO when the file write fails. */
 moe_status moe_register_expert(moe_ctx* ctx, int layer, int expert, const void* blob, size_t bytes);
 
 /* Size in bytes of one expert blob in the boundary format, or 0 for a bad shape. */
@@ -240,6 +256,43 @@ moe_status moe_debug_fail_copies(moe_ctx* ctx, int n);
  * the expected answer.  The time-out is recorded in *status only; it does not make the
  * context sticky. */
 moe_status moe_debug_wait_timeout(moe_ctx* ctx, unsigned long long cycles, void* stream, int* status);
+
+/* ---------------------------------------------------------------- the file tier alone
+ * The RAM + file part of the streamed store on its own ("WISP - streaming what can't run",
+ * section "Insight (Credit: JustVugg / Colibri)": VRAM, then RAM, then SSD, with LRU
+ * promotion), host code only, for host-side tests and tools.  A context created with
+ * moe_config.pool_file uses the same component with pinned RAM slots.
+ * Records of rec_bytes are stored at key * stride, stride = rec_bytes rounded up to 4096;
+ * keys are 0..n_keys-1.  The RAM cache holds floor(ram_bytes / stride) records (at most
+ * n_keys), least recently used evicted first.  Reads of one fetch run on 4 reader threads,
+ * with O_DIRECT where the filesystem allows (moe_filetier_info says which). */
+typedef struct moe_filetier moe_filetier;
+typedef struct {
+    unsigned long long slots;       /* RAM cache records */
+    unsigned long long stride;      /* bytes per record in the file and in RAM */
+    int direct;                     /* 1 = O_DIRECT */
+    unsigned long long reads;       /* records read from the file */
+    unsigned long long read_bytes;
+    unsigned long long ram_hits;    /* fetched keys found in RAM */
+    unsigned long long ram_misses;  /* fetched keys read from the file */
+    double read_ms;                 /* wall time of the read batches */
+} moe_filetier_stats_t;
+
+/* Create (truncate) the file `path` for n_keys records and allocate the RAM cache.
+ * Errors: MOE_EINVAL, MOE_EBUDGET (ram_bytes below one record), MOE_ENOMEM, MOE_EIO. */
+moe_status moe_filetier_create(const char* path, size_t rec_bytes, long long n_keys,
+                               unsigned long long ram_bytes, moe_filetier** out);
+/* Write record `key` (rec_bytes from `rec`, host memory).  A RAM copy of the key is
+ * dropped.  Errors: MOE_EINVAL (bad key, nulls), MOE_EIO. */
+moe_status moe_filetier_write(moe_filetier* ft, long long key, const void* rec);
+/* Make n distinct keys resident in RAM (n <= slots) and return their RAM addresses in
+ * out[n] and slots in slots[n]; they become the most recently used.  The addresses stay
+ * valid until a later fetch or write.  Errors: MOE_EINVAL (n > slots, bad or duplicate
+ * use), MOE_EIO (a read failed; out[] is NULL then). */
+moe_status moe_filetier_fetch(moe_filetier* ft, const long long* keys, int n, const void** out, int* slots);
+moe_status moe_filetier_info(const moe_filetier* ft, moe_filetier_stats_t* out);
+/* Close and free (the file stays; the caller removes it). */
+void moe_filetier_destroy(moe_filetier* ft);
 
 #ifdef __cplusplus
 }

@@ -1,6 +1,6 @@
 """Build the in-tree CUDA libraries for sm_103a (GB300).
 
-``build()`` compiles every ``csrc/*.cu`` of the package into ``libmoe.so`` (the C ABI of
+``build()`` compiles every ``csrc/*.cu`` and ``csrc/*.cpp`` of the package into ``libmoe.so`` (the C ABI of
 include/moe.h) and ``synth/csrc/synth_gen.cu`` into ``synth/libsynthgen.so`` (the
 device fill of the seeded synthetic inputs).  Translation units compile in parallel;
 a library is rebuilt only when a source or header is newer than it.
@@ -48,7 +48,7 @@ def _run(cmd):
 
 
 def build_moe(force: bool = False, verbose: bool = False) -> str:
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     hdrs = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         [os.path.join(ROOT, "include", "moe.h")]
     if not force and not _stale(LIBMOE, srcs + hdrs):
@@ -58,7 +58,7 @@ def build_moe(force: bool = False, verbose: bool = False) -> str:
     objs = []
     jobs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(BUILD, os.path.splitext(os.path.basename(s))[0] + ".o")
         objs.append(o)
         jobs.append([nv] + ARCH + FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", s, "-o", o])
     with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
@@ -66,7 +66,7 @@ def build_moe(force: bool = False, verbose: bool = False) -> str:
             if verbose and r.stderr:
                 print(r.stderr)
     tmp = LIBMOE + ".tmp.%d" % os.getpid()
-    _run([nv] + ARCH + ["-shared", "-o", tmp] + objs)
+    _run([nv] + ARCH + ["-shared", "-o", tmp] + objs + ["-lpthread"])
     os.replace(tmp, LIBMOE)
     return LIBMOE
 

@@ -15,6 +15,9 @@
 //               missed expert's kernels wait only for its own copy, so a copy overlaps
 //               the compute of the experts before it ("WISP", section "Double-Buffer
 //               Async Pipeline").  The shared expert and the routers stay resident.
+//               With a pool file the host pool is itself a cache: every record lives
+//               in the file, and a bounded pinned RAM cache in front of it holds the
+//               recently used ones (filetier.h): VRAM, then RAM, then the file.
 // Caching changes only timing: the kernels compute each expert pass the same way and
 // the combine sums in a fixed order ("Introducing WARP", section "How WARP keeps the
 // model out of RAM": prediction changes timing, never results).
@@ -26,11 +29,13 @@
 #include <cstring>
 #include <list>
 #include <new>
+#include <string>
 #include <unordered_map>
 #include <vector>
 
 #include "../../include/moe.h"
 #include "common.cuh"
+#include "filetier.h"
 #include "kernels.h"
 
 using namespace moe;
@@ -85,7 +90,14 @@ struct moe_ctx {
   uint8_t* d_slab = nullptr;     // resident: [L][E1] records; streamed: slots
   size_t n_slots = 0;
   uint8_t* d_shared = nullptr;   // streamed: [L] shared records
-  uint8_t* h_pool = nullptr;     // streamed: pinned [L][E] records
+  uint8_t* h_pool = nullptr;     // streamed: pinned [L][E] records (no pool file)
+  // pool file: the records in a file behind a pinned RAM cache of ft->slots() records
+  FileTier* ft = nullptr;
+  std::string pool_path;
+  uint8_t* h_ram = nullptr;                  // pinned RAM slots
+  uint8_t* h_wstage = nullptr;               // pinned staging of a registered record
+  std::vector<cudaEvent_t> ram_ev;           // [RAM slot] after the last copy that read it
+  std::vector<char> ram_used;                // that event was recorded
   float* d_router = nullptr;     // [L][E][H]
   std::vector<char> router_ok, expert_ok;
 
@@ -205,6 +217,15 @@ void free_all(moe_ctx* c) {
   cudaFree(c->d_slab);
   cudaFree(c->d_shared);
   if (c->h_pool) cudaFreeHost(c->h_pool);
+  if (c->ft) {
+    delete c->ft;
+    c->ft = nullptr;
+    if (!c->pool_path.empty()) unlink(c->pool_path.c_str());
+  }
+  if (c->h_ram) cudaFreeHost(c->h_ram);
+  if (c->h_wstage) cudaFreeHost(c->h_wstage);
+  for (auto& ev : c->ram_ev) cudaEventDestroy(ev);
+  c->ram_ev.clear();
   cudaFree(c->d_router);
   cudaFree(c->d_rec_table);
   if (c->h_table) cudaFreeHost(c->h_table);
@@ -255,6 +276,7 @@ moe_status validate(const moe_config* g) {
   if (g->router != MOE_ROUTER_SOFTMAX_TOPK_RENORM && g->router != MOE_ROUTER_SIGMOID_TOPK_NORM)
     return MOE_EINVAL;
   if (g->max_tokens < 1 || g->max_tokens > 256) return MOE_EINVAL;
+  if (g->pool_file && (!g->pool_file[0] || g->hbm_cache_bytes == 0)) return MOE_EINVAL;
   if (g->wfmt == MOE_W_RVQ3_G8) {
     if (g->hidden % 8 || g->ffn % 8) return MOE_EINVAL;
   } else if (g->wfmt == MOE_W_INT4_G128) {
@@ -280,6 +302,7 @@ const char* moe_strerror(moe_status s) {
     case MOE_ESTATE: return "layer not fully registered";
     case MOE_ETIMEOUT: return "device wait timed out";
     case MOE_ENOTFOUND: return "nothing recorded yet";
+    case MOE_EIO: return "expert file I/O failed";
   }
   return "unknown status";
 }
@@ -355,7 +378,16 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     slots = std::min(slots, (size_t)L * E);
     c->n_slots = slots;
     expert_bytes = slots * c->rec_bytes + (size_t)L * c->has_shared * c->rec_bytes;
-    const size_t pool = (size_t)L * E * c->rec_bytes;
+    size_t pool = (size_t)L * E * c->rec_bytes;
+    if (cfg->pool_file) {
+      const size_t stride = (c->rec_bytes + FT_ALIGN - 1) / FT_ALIGN * FT_ALIGN;
+      const size_t ram = std::min<size_t>(cfg->host_cache_bytes / stride, (size_t)L * E);
+      if (ram < (size_t)2 * k) {
+        delete c;
+        return MOE_EBUDGET;
+      }
+      pool = ram * stride;
+    }
     const size_t avail = host_available_bytes();
     if (pool + (8ull << 30) > avail) {
       delete c;
@@ -398,9 +430,37 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     if (c->has_shared) AL(c->d_shared, (size_t)L * c->rec_bytes);
     AL(c->d_rec_table, (size_t)(E + 1) * sizeof(uint8_t*));
     AL(c->d_order, (size_t)c->max_pass * sizeof(int));
-    if (cudaHostAlloc((void**)&c->h_pool, (size_t)L * E * c->rec_bytes, cudaHostAllocDefault) !=
-            cudaSuccess ||
-        cudaHostAlloc((void**)&c->h_table, (size_t)(E + 1) * sizeof(uint8_t*), cudaHostAllocDefault) !=
+    if (cfg->pool_file) {
+      const size_t stride = (c->rec_bytes + FT_ALIGN - 1) / FT_ALIGN * FT_ALIGN;
+      const size_t ram = std::min<size_t>(cfg->host_cache_bytes / stride, (size_t)L * E);
+      if (cudaHostAlloc((void**)&c->h_ram, ram * stride, cudaHostAllocDefault) != cudaSuccess ||
+          cudaHostAlloc((void**)&c->h_wstage, stride, cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        free_all(c);
+        delete c;
+        return MOE_ENOMEM;
+      }
+      c->ft = new (std::nothrow) FileTier();
+      c->pool_path = cfg->pool_file;   // removed by free_all, also if open fails half way
+      const int fe = c->ft ? c->ft->open(cfg->pool_file, c->rec_bytes, (long long)L * E, c->h_ram, ram * stride, 8)
+                           : ENOMEM;
+      if (fe != 0) {
+        free_all(c);
+        delete c;
+        return fe == ENOMEM ? MOE_ENOMEM : MOE_EIO;
+      }
+      c->cfg.pool_file = nullptr;   // the caller's string need not outlive the call
+      c->ram_ev.resize(c->ft->slots());
+      for (auto& ev : c->ram_ev) cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      c->ram_used.assign(c->ft->slots(), 0);
+    } else if (cudaHostAlloc((void**)&c->h_pool, (size_t)L * E * c->rec_bytes, cudaHostAllocDefault) !=
+               cudaSuccess) {
+      cudaGetLastError();
+      free_all(c);
+      delete c;
+      return MOE_ENOMEM;
+    }
+    if (cudaHostAlloc((void**)&c->h_table, (size_t)(E + 1) * sizeof(uint8_t*), cudaHostAllocDefault) !=
             cudaSuccess ||
         cudaHostAlloc((void**)&c->h_order, (size_t)c->max_pass * sizeof(int), cudaHostAllocDefault) !=
             cudaSuccess) {
@@ -562,8 +622,15 @@ moe_status moe_register_expert(moe_ctx* c, int layer, int expert, const void* bl
   else dst = c->d_rec_stage;
   CK(launch_repack(c->cfg.wfmt, src, c->cfg.hidden, c->cfg.ffn, dst, c->reg));
   if (c->streamed && expert >= 0) {
-    uint8_t* pool = c->h_pool + ((size_t)layer * E + expert) * c->rec_bytes;
-    CK(cudaMemcpyAsync(pool, dst, c->rec_bytes, cudaMemcpyDeviceToHost, c->reg));
+    const long long fkey = (long long)layer * E + expert;
+    if (c->ft) {
+      CK(cudaMemcpyAsync(c->h_wstage, dst, c->rec_bytes, cudaMemcpyDeviceToHost, c->reg));
+      CK(cudaStreamSynchronize(c->reg));
+      if (c->ft->write(fkey, c->h_wstage) != 0) return MOE_EIO;
+    } else {
+      uint8_t* pool = c->h_pool + ((size_t)layer * E + expert) * c->rec_bytes;
+      CK(cudaMemcpyAsync(pool, dst, c->rec_bytes, cudaMemcpyDeviceToHost, c->reg));
+    }
     // a stale cached copy of this expert must not survive re-registration
     const long long key = (long long)layer * E + expert;
     auto it = c->where.find(key);
@@ -666,6 +733,41 @@ static void forget_slot(moe_ctx* c, int slot) {
   c->slot_prefetched[slot] = 0;
 }
 
+// Host addresses of the records (layer, experts[i]) for i in [i0, i1): the pinned pool, or
+// (pool file) the RAM cache, after reading the absent ones from the file.  A RAM slot is
+// reused only after the last copy that read it has finished.  ram_slot[i] is -1 for the
+// pinned pool.  The batch holds at most ft->slots() records.
+static moe_status host_sources(moe_ctx* c, int layer, const int* experts, int n, const uint8_t** src, int* ram_slot) {
+  const int E = c->cfg.num_experts;
+  if (!c->ft) {
+    for (int i = 0; i < n; ++i) {
+      src[i] = c->h_pool + ((size_t)layer * E + experts[i]) * c->rec_bytes;
+      ram_slot[i] = -1;
+    }
+    return MOE_OK;
+  }
+  std::vector<long long> keys(n);
+  for (int i = 0; i < n; ++i) keys[i] = (long long)layer * E + experts[i];
+  std::vector<uint8_t*> p(n);
+  bool cuda_ok = true;
+  const int fe = c->ft->fetch(keys.data(), n, p.data(), ram_slot, [c, &cuda_ok](int slot) {
+    if (c->ram_used[slot] && cudaEventSynchronize(c->ram_ev[slot]) != cudaSuccess) cuda_ok = false;
+    c->ram_used[slot] = 0;
+  });
+  if (!cuda_ok) return cuda_fail(c);
+  if (fe != 0) return MOE_EIO;
+  for (int i = 0; i < n; ++i) src[i] = p[i];
+  return MOE_OK;
+}
+
+// The copy just queued on cs read RAM slot `slot` (pool file): mark it.
+static moe_status ram_slot_read(moe_ctx* c, int slot, cudaStream_t cs) {
+  if (slot < 0) return MOE_OK;
+  CK(cudaEventRecord(c->ram_ev[slot], cs));
+  c->ram_used[slot] = 1;
+  return MOE_OK;
+}
+
 // ---------------------------------------------------------------- link accounting
 static void batch_drain(moe_ctx* c, bool wait);
 
@@ -756,6 +858,11 @@ static moe_status readahead(moe_ctx* c, int nl, const void* x, int T) {
     if (e >= 0 && e < E && !c->where.count((long long)nl * E + e)) todo.push_back(e);
   }
   if (todo.empty()) return MOE_OK;
+  if (c->ft && (int)todo.size() > c->ft->slots()) todo.resize(c->ft->slots());
+  std::vector<const uint8_t*> srcs(todo.size());
+  std::vector<int> rslot(todo.size());
+  moe_status hs = host_sources(c, nl, todo.data(), (int)todo.size(), srcs.data(), rslot.data());
+  if (hs != MOE_OK) return hs;
   const int ns = (int)std::min<size_t>(moe_ctx::kCopyStreams, todo.size());
   int bi = -1;
   moe_status bs = batch_begin(c, ns, &bi);
@@ -767,12 +874,13 @@ static moe_status readahead(moe_ctx* c, int nl, const void* x, int T) {
     if (slot < 0) break;
     cudaStream_t cs = c->side[m % ns];
     if (c->slot_inflight[slot]) CK(cudaStreamWaitEvent(cs, c->slot_ev[slot], 0));
-    const uint8_t* src = c->h_pool + ((size_t)nl * E + e) * c->rec_bytes;
-    if (cudaMemcpyAsync(c->d_slab + (size_t)slot * c->rec_bytes, src, c->rec_bytes, cudaMemcpyHostToDevice, cs) !=
-        cudaSuccess) {
+    if (cudaMemcpyAsync(c->d_slab + (size_t)slot * c->rec_bytes, srcs[m], c->rec_bytes, cudaMemcpyHostToDevice,
+                        cs) != cudaSuccess) {
       forget_slot(c, slot);
       return cuda_fail(c);
     }
+    moe_status rs = ram_slot_read(c, rslot[m], cs);
+    if (rs != MOE_OK) return rs;
     CK(cudaEventRecord(c->slot_ev[slot], cs));
     c->slot_inflight[slot] = 1;
     c->slot_prefetched[slot] = 1;
@@ -948,10 +1056,23 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     moe_status bs = batch_begin(c, ns, &bi);
     if (bs != MOE_OK) return bs;
   }
+  // sources: the pinned pool, or the RAM cache in chunks of at most its size (a later
+  // chunk's reads wait for the copies of an earlier one only where they reuse its slots)
+  const size_t chunk = c->ft ? (size_t)c->ft->slots() : std::max<size_t>(1, miss_experts.size());
+  std::vector<const uint8_t*> srcs(miss_experts.size());
+  std::vector<int> rslot(miss_experts.size(), -1);
   for (size_t m = 0; m < miss_experts.size(); ++m) {
     cudaStream_t cs = c->side[m % ns];
     const int e = miss_experts[m], slot = miss_slot[m];
-    const uint8_t* src = c->h_pool + ((size_t)layer * E + e) * c->rec_bytes;
+    if (m % chunk == 0) {
+      const int n = (int)std::min(chunk, miss_experts.size() - m);
+      moe_status hs = host_sources(c, layer, miss_experts.data() + m, n, srcs.data() + m, rslot.data() + m);
+      if (hs != MOE_OK) {
+        for (size_t q = m; q < miss_experts.size(); ++q) forget_slot(c, miss_slot[q]);   // never filled
+        return hs;
+      }
+    }
+    const uint8_t* src = srcs[m];
     // a read-ahead copy into the victim slot may still be running: this one goes after it
     if (c->slot_inflight[slot]) CK(cudaStreamWaitEvent(cs, c->slot_ev[slot], 0));
     c->slot_inflight[slot] = 0;
@@ -966,6 +1087,8 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
       forget_slot(c, slot);  // the slot's content is unknown now
       return cuda_fail(c);
     }
+    moe_status rs = ram_slot_read(c, rslot[m], cs);
+    if (rs != MOE_OK) return rs;
     CK(cudaEventRecord(c->copy_ev[m], cs));
     c->bytes_h2d += c->rec_bytes;
   }
@@ -1074,6 +1197,14 @@ moe_status moe_stats(moe_ctx* c, moe_stats_t* out) {
   out->h2d_ms = c->h2d_ms;
   out->prefetches = c->prefetches;
   out->prefetch_hits = c->prefetch_hits;
+  if (c->ft) {
+    out->file_reads = c->ft->reads;
+    out->file_read_bytes = c->ft->read_bytes;
+    out->ram_hits = c->ft->ram_hits;
+    out->ram_misses = c->ft->ram_misses;
+    out->file_read_ms = c->ft->read_ms;
+    out->file_direct = c->ft->direct() ? 1 : 0;
+  }
   return st;
 }
 
@@ -1087,6 +1218,10 @@ moe_status moe_reset_stats(moe_ctx* c) {
   c->hits = c->misses = c->bytes_h2d = 0;
   c->prefetches = c->prefetch_hits = 0;
   c->h2d_ms = 0.0;
+  if (c->ft) {
+    c->ft->reads = c->ft->read_bytes = c->ft->ram_hits = c->ft->ram_misses = 0;
+    c->ft->read_ms = 0.0;
+  }
   return MOE_OK;
 }
 

@@ -12,7 +12,7 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIBMOE = os.path.join(PKG, "libmoe.so")
 
-OK, EINVAL, ENOMEM, EBUDGET, ECUDA, ESTATE, ETIMEOUT, ENOTFOUND = range(8)
+OK, EINVAL, ENOMEM, EBUDGET, ECUDA, ESTATE, ETIMEOUT, ENOTFOUND, EIO = range(9)
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 W_RVQ3, W_INT4 = 1, 2
 
@@ -29,14 +29,26 @@ class Config(ctypes.Structure):
         ("num_experts", ctypes.c_int), ("top_k", ctypes.c_int), ("shared_ffn", ctypes.c_int),
         ("router", ctypes.c_int), ("wfmt", ctypes.c_int), ("max_tokens", ctypes.c_int),
         ("hbm_cache_bytes", ctypes.c_ulonglong),
+        ("pool_file", ctypes.c_char_p), ("host_cache_bytes", ctypes.c_ulonglong),
     ]
+
+
+class FileTierStats(ctypes.Structure):
+    _fields_ = [("slots", ctypes.c_ulonglong), ("stride", ctypes.c_ulonglong), ("direct", ctypes.c_int),
+                ("reads", ctypes.c_ulonglong), ("read_bytes", ctypes.c_ulonglong),
+                ("ram_hits", ctypes.c_ulonglong), ("ram_misses", ctypes.c_ulonglong), ("read_ms", ctypes.c_double)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_ulonglong) for n in (
         "forwards", "tokens", "lookups", "hits", "misses", "bytes_expert_touched",
         "bytes_router", "bytes_h2d", "record_bytes", "cache_slots")] + [("h2d_ms", ctypes.c_double)] + [
-        (n, ctypes.c_ulonglong) for n in ("prefetches", "prefetch_hits")]
+        (n, ctypes.c_ulonglong) for n in ("prefetches", "prefetch_hits", "file_reads", "file_read_bytes",
+                                          "ram_hits", "ram_misses")] + [
+        ("file_read_ms", ctypes.c_double), ("file_direct", ctypes.c_int)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -74,11 +86,19 @@ def lib():
     L.moe_debug_fail_copies.argtypes = [vp, i]
     L.moe_set_readahead.argtypes = [vp, i]
     L.moe_debug_wait_timeout.argtypes = [vp, u64, vp, ctypes.POINTER(i)]
+    L.moe_filetier_create.argtypes = [ctypes.c_char_p, ctypes.c_size_t, ctypes.c_longlong, u64, ctypes.POINTER(vp)]
+    L.moe_filetier_write.argtypes = [vp, ctypes.c_longlong, vp]
+    L.moe_filetier_fetch.argtypes = [vp, ctypes.POINTER(ctypes.c_longlong), i, ctypes.POINTER(vp),
+                                     ctypes.POINTER(i)]
+    L.moe_filetier_info.argtypes = [vp, ctypes.POINTER(FileTierStats)]
+    L.moe_filetier_destroy.argtypes = [vp]
+    L.moe_filetier_destroy.restype = None
     for name in ("moe_create", "moe_register_router", "moe_register_expert", "moe_forward",
                  "moe_get_routing", "moe_residual_rmsnorm", "moe_stats", "moe_reset_stats",
                  "moe_destroy", "moe_debug_fail_copies", "moe_debug_wait_timeout",
                  "moe_profile", "moe_profile_read", "moe_forward_residual", "moe_route_noalloc",
-                 "moe_set_readahead"):
+                 "moe_set_readahead", "moe_filetier_create", "moe_filetier_write", "moe_filetier_fetch",
+                 "moe_filetier_info"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -120,13 +140,63 @@ def route_noalloc(x_bf16, W, T, H, E, k, router, idx, w, stream=None):
         raise MoeError(st, "moe_route_noalloc")
 
 
+class FileTier:
+    """The RAM + file tier on its own (moe_filetier_*): host memory only, no GPU."""
+
+    def __init__(self, path, rec_bytes, n_keys, ram_bytes):
+        h = ctypes.c_void_p()
+        st = lib().moe_filetier_create(str(path).encode(), rec_bytes, n_keys, ram_bytes, ctypes.byref(h))
+        if st != OK:
+            raise MoeError(st, "moe_filetier_create")
+        self._h = h
+        self.rec_bytes = rec_bytes
+
+    def write(self, key, rec):
+        """rec: a contiguous numpy uint8 array of rec_bytes."""
+        assert rec.nbytes == self.rec_bytes
+        st = lib().moe_filetier_write(self._h, key, rec.ctypes.data)
+        if st != OK:
+            raise MoeError(st, "moe_filetier_write")
+
+    def fetch(self, keys):
+        """Returns (list of record bytes copies, list of RAM slots)."""
+        n = len(keys)
+        karr = (ctypes.c_longlong * n)(*keys)
+        out = (ctypes.c_void_p * n)()
+        slots = (ctypes.c_int * n)()
+        st = lib().moe_filetier_fetch(self._h, karr, n, out, slots)
+        if st != OK:
+            raise MoeError(st, "moe_filetier_fetch")
+        recs = [ctypes.string_at(out[i], self.rec_bytes) for i in range(n)]
+        return recs, list(slots)
+
+    def info(self):
+        s = FileTierStats()
+        st = lib().moe_filetier_info(self._h, ctypes.byref(s))
+        if st != OK:
+            raise MoeError(st, "moe_filetier_info")
+        return s.as_dict()
+
+    def close(self):
+        if self._h:
+            lib().moe_filetier_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Context:
     """One stack of MoE layers on one GPU (wraps moe_ctx)."""
 
     def __init__(self, num_layers, hidden, ffn, num_experts, top_k, wfmt, router=ROUTER_SOFTMAX,
-                 shared_ffn=0, max_tokens=1, hbm_cache_bytes=0, device=0):
+                 shared_ffn=0, max_tokens=1, hbm_cache_bytes=0, device=0, pool_file=None, host_cache_bytes=0):
         self.cfg = Config(num_layers, hidden, ffn, num_experts, top_k, shared_ffn, router, wfmt,
-                          max_tokens, hbm_cache_bytes)
+                          max_tokens, hbm_cache_bytes,
+                          pool_file.encode() if pool_file else None, host_cache_bytes)
         self.device = device
         h = ctypes.c_void_p()
         st = lib().moe_create(ctypes.byref(self.cfg), device, ctypes.byref(h))

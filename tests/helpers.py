@@ -31,11 +31,12 @@ class LayerSpec:
         return S.make_router(self.seed, layer, self.E, self.H)
 
 
-def make_context(spec, max_tokens, hbm_cache_bytes=0, register=True, order=None):
+def make_context(spec, max_tokens, hbm_cache_bytes=0, register=True, order=None, pool_file=None,
+                 host_cache_bytes=0):
     import routed_expert_ffn_03_gb300 as M
     ctx = M.Context(spec.layers, spec.H, spec.F, spec.E, spec.k, spec.wfmt, router=spec.router,
                     shared_ffn=spec.F if spec.shared else 0, max_tokens=max_tokens,
-                    hbm_cache_bytes=hbm_cache_bytes)
+                    hbm_cache_bytes=hbm_cache_bytes, pool_file=pool_file, host_cache_bytes=host_cache_bytes)
     if register:
         for l in range(spec.layers):
             ctx.register_router(l, spec.router_w(l))

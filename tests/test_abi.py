@@ -65,3 +65,14 @@ def test_null_arguments(lib):
     assert lib.moe_forward(None, 0, None, None, 1, None) == M.EINVAL
     assert lib.moe_destroy(None) == M.OK
     assert M.strerror(M.EBUDGET)
+
+
+def test_pool_file_needs_the_streamed_mode(lib):
+    import routed_expert_ffn_03_gb300 as M
+    h = ctypes.c_void_p()
+    cfg = M.Config(1, 256, 128, 8, 2, 0, 0, M.W_INT4, 1, 0, b"/tmp/unused-pool.bin", 1 << 30)
+    assert lib.moe_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == M.EINVAL   # no HBM cache budget
+    cfg = M.Config(1, 256, 128, 8, 2, 0, 0, M.W_INT4, 1, 1 << 30, b"", 1 << 30)
+    assert lib.moe_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == M.EINVAL   # empty path
+    assert not h.value
+    assert M.strerror(M.EIO)

@@ -46,6 +46,36 @@ def _tokens(spec, n, T=1):
 
 
 @pytest.mark.parametrize("spec", [SPEC, SPEC4])
+def test_file_tier_streamed_equals_resident_bitwise(spec, tmp_path):
+    """Experts in a file behind a RAM cache of 2k + 1 records, behind an HBM cache of 2k
+    slots: VRAM, then RAM, then the file; the results are those of the all-resident run."""
+    import os
+    seq = _tokens(spec, 10)
+    ref_ctx = make_context(spec, 1)
+    ref, ref_routes = _stack_run(ref_ctx, spec, seq)
+    ref_ctx.close()
+    probe = make_context(spec, 1, hbm_cache_bytes=1 << 40, register=False)
+    rb = probe.stats()["record_bytes"]
+    probe.close()
+    stride = (rb + 4095) // 4096 * 4096
+    path = str(tmp_path / "experts.bin")
+    for readahead in (0, 1):
+        ctx = make_context(spec, 1, hbm_cache_bytes=2 * spec.k * rb, pool_file=path,
+                           host_cache_bytes=(2 * spec.k + 1) * stride)
+        assert os.path.getsize(path) == spec.layers * spec.E * stride
+        ctx.set_readahead(bool(readahead))
+        out, routes = _stack_run(ctx, spec, seq)
+        st = ctx.stats()
+        ctx.close()
+        assert not os.path.exists(path)          # the context removes its file
+        assert st["misses"] > 0 and st["ram_misses"] > 0 and st["file_reads"] == st["ram_misses"]
+        assert st["file_read_bytes"] == st["file_reads"] * stride
+        np.testing.assert_array_equal(out, ref)
+        for a, b in zip(routes, ref_routes):
+            np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("spec", [SPEC, SPEC4])
 def test_streamed_equals_resident_bitwise(spec):
     import routed_expert_ffn_03_gb300 as M
     seq = _tokens(spec, 12)

@@ -1048,6 +1048,15 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   CK(cudaMemcpyAsync(c->d_rec_table, c->h_table, (size_t)(E + 1) * sizeof(uint8_t*),
                      cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(c->d_order, c->h_order, (size_t)n_pass * sizeof(int), cudaMemcpyHostToDevice, s));
+  // the ready experts' kernels go first, so they run while the host reads missed records
+  // from the file (file tier) and queues their copies
+  ExpertArgs a = expert_args(c, c->d_rec_table, x, T);
+  a.range.order = c->d_order;
+  if (n_first > 0) {
+    a.range.p_begin = 0;
+    a.range.p_end = n_first;
+    CK(launch_experts(c, a, s));
+  }
 
   // miss copies on the side streams (round-robin), in ascending expert id, one event each
   const int ns = (int)std::min<size_t>(moe_ctx::kCopyStreams, std::max<size_t>(1, miss_experts.size()));
@@ -1097,13 +1106,6 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     if (be != MOE_OK) return be;
   }
 
-  ExpertArgs a = expert_args(c, c->d_rec_table, x, T);
-  a.range.order = c->d_order;
-  if (n_first > 0) {
-    a.range.p_begin = 0;
-    a.range.p_end = n_first;
-    CK(launch_experts(c, a, s));
-  }
   for (size_t m = 0; m < group_experts.size(); ++m) {
     if (m < wait_experts.size()) {
       const int slot = wait_slot[m];

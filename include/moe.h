@@ -67,7 +67,8 @@ typedef enum {
     MOE_OK = 0,
     MOE_EINVAL = 1,     /* bad argument (null, out of range, size mismatch) */
     MOE_ENOMEM = 2,     /* HBM or pinned host memory could not be allocated */
-    MOE_EBUDGET = 3,    /* the HBM cache cannot hold one layer's working set (2 k records) */
+    MOE_EBUDGET = 3,    /* the HBM cache cannot hold one layer's working set
+                           (max(2 k, min(E, max_tokens k)) records) */
     MOE_ECUDA = 4,      /* a CUDA call failed (sticky) */
     MOE_ESTATE = 5,     /* a router or expert of the layer is not registered yet */
     MOE_ETIMEOUT = 6,   /* a bounded device wait ran out (sticky) */
@@ -139,7 +140,8 @@ typedef struct moe_ctx moe_ctx;
  * the pinned host pool (streamed mode only: every expert, or with pool_file the RAM
  * cache in front of the expert file), router storage and scratch.
  * Errors: MOE_EINVAL (bad config; pool_file without hbm_cache_bytes), MOE_EBUDGET (HBM
- * cache below 2 k records, or above what the pool needs is allowed and clipped; RAM cache
+ * cache below max(2 k, min(E, max_tokens k)) records, a forward's worst-case working set
+ * beside the next layer's; above what the pool needs is allowed and clipped; RAM cache
  * below 2 k records), MOE_ENOMEM (HBM or host memory short; checked against
  * cudaMemGetInfo before allocating), MOE_EIO (the expert file), MOE_ECUDA. */
 moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out);

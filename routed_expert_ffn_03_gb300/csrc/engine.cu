@@ -370,8 +370,10 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   if (!c->streamed) {
     expert_bytes = (size_t)L * c->E1 * c->rec_bytes;
   } else {
+    // a forward pins all its unique experts, at most min(E, max_tokens k) of them, and
+    // the next layer's must find room beside the current one's: 2 k at T = 1
     size_t slots = cfg->hbm_cache_bytes / c->rec_bytes;
-    if (slots < (size_t)2 * k) {
+    if (slots < std::max((size_t)2 * k, std::min((size_t)E, (size_t)maxT * k))) {
       delete c;
       return MOE_EBUDGET;
     }
@@ -995,6 +997,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   const int* pexp = rb + 8 + E;
 
   // lookups: hits, hits whose read-ahead copy may still be running, misses
+  if (n_uniq < 0 || (size_t)n_uniq > c->n_slots) return MOE_EBUDGET;  // create sized the slots for this
   for (size_t i = 0; i < c->n_slots; ++i) c->slot_pinned[i] = 0;
   std::vector<int> miss_experts, miss_slot, wait_experts, wait_slot;
   std::vector<char> grouped(E, 0);
@@ -1002,7 +1005,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     const int e = uniq[i];
     bool hit = false;
     const int slot = cache_get(c, (long long)layer * E + e, &hit);
-    if (slot < 0) return MOE_EBUDGET;  // cannot happen: slots >= 2k >= unique experts
+    if (slot < 0) return MOE_EBUDGET;  // cannot happen: the pinned ones are fewer than the slots
     c->slot_pinned[slot] = 1;
     c->h_table[e] = c->d_slab + (size_t)slot * c->rec_bytes;
     if (hit) {

@@ -143,6 +143,38 @@ def test_cache_below_two_k_records_is_refused():
     assert ei.value.status == M.EBUDGET
 
 
+@pytest.mark.parametrize("spec", [SPEC, SPEC4])
+def test_multi_token_streamed_equals_resident_bitwise(spec, tmp_path):
+    """T = 4: a forward may pin min(E, 4 k) experts, so the HBM cache needs that many
+    slots (one fewer is refused at create).  With exactly that many, and with the file
+    tier's RAM cache (2 k + 1 records) smaller than a forward's misses (read in chunks),
+    the results are those of the all-resident run."""
+    import routed_expert_ffn_03_gb300 as M
+    T = 4
+    seq = _tokens(spec, 6, T)
+    ref_ctx = make_context(spec, T)
+    ref, ref_routes = _stack_run(ref_ctx, spec, seq)
+    ref_ctx.close()
+    probe = make_context(spec, T, hbm_cache_bytes=1 << 40, register=False)
+    rb = probe.stats()["record_bytes"]
+    probe.close()
+    need = max(2 * spec.k, min(spec.E, T * spec.k))
+    with pytest.raises(M.MoeError) as ei:
+        make_context(spec, T, hbm_cache_bytes=(need - 1) * rb, register=False)
+    assert ei.value.status == M.EBUDGET
+    stride = (rb + 4095) // 4096 * 4096
+    for pool_file in (None, str(tmp_path / "experts.bin")):
+        ctx = make_context(spec, T, hbm_cache_bytes=need * rb, pool_file=pool_file,
+                           host_cache_bytes=(2 * spec.k + 1) * stride if pool_file else 0)
+        out, routes = _stack_run(ctx, spec, seq)
+        st = ctx.stats()
+        ctx.close()
+        assert st["misses"] > 0
+        np.testing.assert_array_equal(out, ref)
+        for a, b in zip(routes, ref_routes):
+            np.testing.assert_array_equal(a, b)
+
+
 def test_forward_before_registration_and_bad_args():
     import torch
     import routed_expert_ffn_03_gb300 as M

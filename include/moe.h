@@ -101,7 +101,9 @@ typedef struct {
     const char* pool_file;              /* streamed mode: NULL = the host pool holds every
                                            expert in pinned RAM; else the experts live in this
                                            file (created, truncated, removed by moe_destroy)
-                                           behind a pinned RAM cache of host_cache_bytes */
+                                           behind a pinned RAM cache of host_cache_bytes;
+                                           read by MOE_FILE_READERS threads (env, 1..64,
+                                           default 8) */
     unsigned long long host_cache_bytes; /* with pool_file: the RAM cache budget in bytes
                                             (at least 2 k records of 4096-byte aligned size) */
 } moe_config;

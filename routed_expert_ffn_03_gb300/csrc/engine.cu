@@ -26,6 +26,7 @@
 
 #include <chrono>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <list>
 #include <new>
@@ -444,7 +445,11 @@ moe_status moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       }
       c->ft = new (std::nothrow) FileTier();
       c->pool_path = cfg->pool_file;   // removed by free_all, also if open fails half way
-      const int fe = c->ft ? c->ft->open(cfg->pool_file, c->rec_bytes, (long long)L * E, c->h_ram, ram * stride, 8)
+      // reader threads: MOE_FILE_READERS (1..64) where set, else 8
+      int readers = 8;
+      if (const char* env = getenv("MOE_FILE_READERS")) readers = std::min(64, std::max(1, atoi(env)));
+      const int fe = c->ft ? c->ft->open(cfg->pool_file, c->rec_bytes, (long long)L * E, c->h_ram, ram * stride,
+                                         readers)
                            : ENOMEM;
       if (fe != 0) {
         free_all(c);

@@ -1,24 +1,28 @@
 #!/usr/bin/env python3
 """Benchmark of the decode-time routed MoE layer stack on GB300 (one JSON line).
 
-Default workload: the Mixtral-shaped stack - 32 MoE layers, H = 4096, F = 14336, 8 experts
-per layer, top-2 softmax router, int4 experts (symmetric, group 128, fp16 scales; 90.8 MB
-per expert, 256 experts = 23 GB resident in HBM), decode T = 1, a 512-token sequence of
-x ~ N(0,1) (bf16) fed layer to layer as x += moe(rmsnorm(x)).  One step = one token
-through all 32 layers (router, gate/up, down, combine and the residual RMS norm of every
-layer), replayed from one CUDA graph with the inputs resident in HBM.  The per-token
-expert working set (2 x 32 x 90.8 MB = 5.8 GB) is far larger than the 129 MB L2, so no
-flush is needed between steps.
+Default workload: the DeepSeek-V3-shaped stack, the largest that fits one GPU - 58 MoE
+layers, H = 7168, 256 routed experts with F = 2048 plus one always-on shared expert,
+sigmoid scores with top-8 selected and normalised, RVQ 3-bit experts (16.55 MB per expert,
+58 x 257 experts = 246.7 GB resident in HBM), decode T = 1, x ~ N(0,1) (bf16) fed layer to
+layer as x += moe(rmsnorm(x)).  One step = one token through all 58 layers (router,
+gate/up, down, combine and the residual RMS norm of every layer), replayed from one CUDA
+graph with the inputs resident in HBM.  The per-token expert working set (9 x 58 x
+16.55 MB = 8.6 GB) is far larger than the 129 MB L2, so no flush is needed between steps.
 
-Other workloads (``--config``): tiny, dsv3 (T = 1, 4 or 32 via --tokens-per-step),
-wide, stream (HBM LRU cache over a pinned host pool).
+Other workloads (``--config``): tiny, mixtral (32 int4 layers), dsv3 with T = 4 or 32
+(--tokens-per-step), wide, stream (HBM LRU cache over a pinned host pool), stream-file;
+``--top-k`` overrides k (the streamed top-16 vs top-8 comparison).
 
 Reported: tokens/s (value), expert-weight GB/s against the HBM peak, hit %, the dominant
 kernel's roofline (CUDA events around each kernel, recorded inside the timed graph), the
 end-to-end rate through host buffers, SM clocks sampled during the timed region, and the
-fp64 CPU oracle timed on a bounded sample (``cpu_baseline``).  ``--impl reference`` times
-that oracle alone on the same workload.  N > 1 GPUs (torchrun) run independent replicas:
-the layer does not shard (weak scaling, no collective on the data path).
+fp64 CPU oracle timed on a bounded sample (``cpu_baseline``), which also routes the GPU
+run's own normalised inputs of a few tokens and reports the near-ties (oracle gap between
+the k-th and (k+1)-th score below 1e-5) and any expert-id mismatch outside them.
+``--impl reference`` times that oracle alone on the same workload.  N > 1 GPUs (torchrun)
+run independent replicas: the layer does not shard (weak scaling, no collective on the
+data path).
 """
 from __future__ import annotations
 
@@ -262,17 +266,46 @@ def oracle_layer_sample(cfg, n_tokens, n_layers, device):
     return dt, O.threads()
 
 
-def cpu_baseline(cfg, device):
+def routing_check(cfg, check):
+    """The oracle router (fp64 logits, brute-force top-k) on the normalised inputs the GPU
+    run fed each layer (teacher-forced): counts the near-ties (oracle gap between the k-th
+    and (k+1)-th score below 1e-5) and the decisions whose expert ids differ outside them."""
+    from oracle import oracle as O
+    routers = {}
+    n = ties = flips = mism = 0
+    t0 = time.perf_counter()
+    for per_xn, per_idx in check:
+        for l, (xnb, idx) in enumerate(zip(per_xn, per_idx)):
+            if l not in routers:
+                routers[l] = S.make_router(SEED, l, cfg["E"], cfg["H"])
+            r = O.router(xnb, routers[l], cfg["k"], cfg["router"])
+            for t in range(xnb.shape[0]):
+                n += 1
+                same = np.array_equal(idx[t], r["idx"][t])
+                if r["gap"][t] < 1e-5:
+                    ties += 1
+                    flips += 0 if same else 1
+                elif not same:
+                    mism += 1
+    return {"decisions": n, "near_ties": ties, "near_tie_flips": flips, "mismatches_outside_near_ties": mism,
+            "sample": "the GPU run's bf16 router inputs of %d steps x %d layers x %d tokens per step, routed by the "
+                      "fp64 oracle (%.1f s)" % (len(check), cfg["layers"], cfg["T"], time.perf_counter() - t0)}
+
+
+def cpu_baseline(cfg, device, check=None):
     n_tok, n_lay = (4, min(cfg["layers"], 8)) if cfg["wfmt"] == S.INT4 else (2, min(cfg["layers"], 4))
     if cfg["name"] == "tiny":
         n_tok, n_lay = 4, 1
     dt, cores = oracle_layer_sample(cfg, n_tok, n_lay, device)
     per_token = dt / n_tok * cfg["layers"] / n_lay
-    return {"value": cfg["T"] / per_token if cfg["T"] > 1 and cfg["name"] == "tiny" else 1.0 / per_token,
-            "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": "fp64 oracle (router, top-k, explicit dequant, dense SwiGLU, combine, rmsnorm stack) on "
-                      "%d tokens x the first %d of %d layers, %.1f s, extrapolated to the full stack"
-                      % (n_tok, n_lay, cfg["layers"], dt)}
+    out = {"value": cfg["T"] / per_token if cfg["T"] > 1 and cfg["name"] == "tiny" else 1.0 / per_token,
+           "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": "fp64 oracle (router, top-k, explicit dequant, dense SwiGLU, combine, rmsnorm stack) on "
+                     "%d tokens x the first %d of %d layers, %.1f s, extrapolated to the full stack"
+                     % (n_tok, n_lay, cfg["layers"], dt)}
+    if check:
+        out["routing_check"] = routing_check(cfg, check)
+    return out
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -462,7 +495,10 @@ def run_gpu(args, cfg, rank, world, device):
                         "traffic": tr, "peak_source": peak_src,
                         "alg_bytes_per_launch": int(alg), "avg_launch_us": round(dur * 1e6, 2),
                         "timing": "CUDA events around each kernel on its stream, %d replays x %d layers "
-                                  "(event nodes in a separate copy of the step graph)" % (args.prof_steps, cfg["layers"]),
+                                  "(event nodes in a separate copy of the step graph); an event node between two "
+                                  "kernels chained by programmatic dependent launch stops the next kernel's prologue "
+                                  "from overlapping the previous one's tail, so this duration is an upper bound and "
+                                  "the fraction a lower bound" % (args.prof_steps, cfg["layers"]),
                         "per_kernel_us": {n: round(v / nl * 1e3, 2) for n, v in
                                           zip(("router", "gateup", "down", "combine"), ms4)}}
     out = {
@@ -519,9 +555,28 @@ def run_gpu(args, cfg, rank, world, device):
                 "read_measure": "records read from the file (4096-byte aligned, 8 reader threads) / wall time of "
                                 "the read batches, which the forward waits for"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the router inputs (bf16 xn) and expert ids of every layer for a few steps, read back
+        # layer by layer, for the oracle's routing check in the CPU-baseline leg
+        check = []
+        if streamed:
+            ctx.set_readahead(False)
+        with torch.cuda.stream(stream):
+            for i in range(args.check_tokens):
+                x.copy_(x0_dev[i % n_inp])
+                per_xn, per_idx = [], []
+                for l in range(L):
+                    ctx.forward_residual(l, x, None if l == 0 else y, xn, y, T)
+                    per_xn.append(xn.cpu().numpy().view(np.uint16).copy())
+                    per_idx.append(ctx.get_routing(l)[0])
+                check.append((per_xn, per_idx))
+        torch.cuda.synchronize()
         ctx.close()
         torch.cuda.empty_cache()
-        out["cpu_baseline"] = cpu_baseline(cfg, device)
+        out["cpu_baseline"] = cpu_baseline(cfg, device, check)
+        rc = out["cpu_baseline"].get("routing_check")
+        if rc:
+            out["near_ties"] = {k_: rc[k_] for k_ in ("decisions", "near_ties", "near_tie_flips",
+                                                      "mismatches_outside_near_ties")}
     else:
         ctx.close()
     return out
@@ -533,22 +588,14 @@ def run_reference(args, cfg, device):
     expert of one layer (layers cycle over the first few), so the whole run stays within
     minutes; the rate is extrapolated to the full stack."""
     from oracle import oracle as O
-    import torch
-    from synth import device as D
     nl = min(cfg["layers"], 2)
     xin = token_inputs(cfg, max(1, min(cfg["tokens"], 64)))
     routers = [S.make_router(SEED, l, cfg["E"], cfg["H"]) for l in range(nl)]
-    nb = S.expert_blob_bytes(cfg["wfmt"], cfg["H"], cfg["F"])
-    dev = torch.empty(nb, dtype=torch.uint8, device="cuda:%d" % device) if torch.cuda.is_available() else None
     cache = {}
 
-    def blob(l, e):
+    def blob(l, e):       # host generator: this arm loads no GPU library
         if (l, e) not in cache:
-            if dev is not None:
-                D.make_expert_blob_device(SEED, l, e, cfg["wfmt"], cfg["H"], cfg["F"], dev)
-                cache[(l, e)] = dev.cpu().numpy()
-            else:
-                cache[(l, e)] = S.make_expert_blob(SEED, l, e, cfg["wfmt"], cfg["H"], cfg["F"])
+            cache[(l, e)] = S.make_expert_blob(SEED, l, e, cfg["wfmt"], cfg["H"], cfg["F"])
         return cache[(l, e)]
 
     shapes = S.matrix_shapes(cfg["H"], cfg["F"])
@@ -599,8 +646,11 @@ def main():
     ap.add_argument("--steps", type=int, default=1024)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="mixtral", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="dsv3", choices=sorted(CONFIGS))
     ap.add_argument("--tokens-per-step", type=int, default=0, help="override T (dsv3: 1, 4, 32)")
+    ap.add_argument("--top-k", type=int, default=0, help="override k (e.g. 8 on the top-16 stream config)")
+    ap.add_argument("--check-tokens", type=int, default=8,
+                    help="tokens whose per-layer normalised inputs the CPU-baseline leg routes with the oracle")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prof-steps", type=int, default=16, help="replays of the per-kernel event graph")
     ap.add_argument("--readahead", type=int, default=1, choices=[0, 1],
@@ -618,6 +668,11 @@ def main():
     if args.tokens_per_step:
         cfg["T"] = args.tokens_per_step
         cfg["workload"] += " (T=%d per step)" % cfg["T"]
+    if args.top_k:
+        if not 1 <= args.top_k <= min(cfg["E"], 32):
+            raise SystemExit("--top-k must be in 1..%d" % min(cfg["E"], 32))
+        cfg["workload"] += " (top-%d instead of top-%d)" % (args.top_k, cfg["k"])
+        cfg["k"] = args.top_k
     if cfg.get("host_cache"):
         # the file tier: the expert file goes to --pool-file's directory (default: the temp
         # directory); fewer layers when that filesystem lacks room for all of them
@@ -642,8 +697,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        import __graft_entry__ as G
-        G.build()
+        from oracle import oracle as O      # builds and loads oracle/liboracle.so only
+        O.build()
         print(json.dumps(run_reference(args, cfg, local)), flush=True)
         return
 

@@ -268,8 +268,9 @@ moe_status moe_debug_wait_timeout(moe_ctx* ctx, unsigned long long cycles, void*
  * moe_config.pool_file uses the same component with pinned RAM slots.
  * Records of rec_bytes are stored at key * stride, stride = rec_bytes rounded up to 4096;
  * keys are 0..n_keys-1.  The RAM cache holds floor(ram_bytes / stride) records (at most
- * n_keys), least recently used evicted first.  Reads of one fetch run on 4 reader threads,
- * with O_DIRECT where the filesystem allows (moe_filetier_info says which). */
+ * n_keys), least recently used evicted first.  Reads of one fetch run on MOE_FILE_READERS
+ * reader threads (env, 1..64, default 8), with O_DIRECT where the filesystem allows
+ * (moe_filetier_info says which). */
 typedef struct moe_filetier moe_filetier;
 typedef struct {
     unsigned long long slots;       /* RAM cache records */

@@ -350,3 +350,79 @@ def test_rvq_is_three_bits_per_weight():
     H, F = 7168, 1536
     code_bytes = O.expert_bytes(RVQ, H, F) - 3 * 3 * 256 * 8 * 2
     assert code_bytes * 8 == 3 * (3 * H * F)
+
+
+# ---------------------------------------------------------------- combine and stack in closed form
+SG, SU, SD = 2.0 ** -7, 2.0 ** -6, 2.0 ** -9      # exact fp16 scales
+
+
+def _const_expert_value(X, F, cg, cu, cd, sg=SG, su=SU, sd=SD):
+    """Every output row of an int4 expert whose gate/up/down codes are the constants cg, cu,
+    cd (one scale per matrix), on an input whose entries sum to X: g = cg sg X, u = cu su X
+    in every row, h = silu(g) u, y = cd sd F h (silu from scipy's logistic)."""
+    g, u = cg * sg * X, cu * su * X
+    return cd * sd * F * (g * expit(g) * u)
+
+
+@pytest.mark.parametrize("kind", [O.SOFTMAX, O.SIGMOID])
+def test_weighted_combine_unequal_weights_closed_form(kind):
+    """k = 2 of 3 experts with unequal weights: y = w_a y_a + w_b y_b written out by hand.
+
+    Router row e is a_e at input 0 and zero elsewhere, and x = (1, 0.5, 0, ...), so the
+    logits are exactly a = (0.5, -0.25, 1.0): expert 2 ranks first, expert 0 second.
+    Softmax renormalised over the two: w = (1, e^-0.5) / (1 + e^-0.5); sigmoid normalised:
+    w = (s(1), s(0.5)) / (s(1) + s(0.5)).  The three experts have different constant codes,
+    so pairing a weight with the wrong expert, or the wrong rank order, changes y."""
+    H = F = 128
+    consts = {0: (3, -2, 5), 1: (-1, 4, 2), 2: (2, 3, -4)}
+    blobs = {e: _int4_expert_blob(H, F, *c, SG, SU, SD) for e, c in consts.items()}
+    x = np.zeros((1, H))
+    x[0, 0], x[0, 1] = 1.0, 0.5
+    X = 1.5
+    Wr = np.zeros((3, H), np.float32)
+    Wr[:, 0] = [0.5, -0.25, 1.0]
+    r = O.layer(bits(x), Wr, 2, kind, blobs.__getitem__, INT4, H, F)
+    if kind == O.SOFTMAX:
+        w_first = 1.0 / (1.0 + math.exp(-0.5))
+    else:
+        s1, s05 = 1 / (1 + math.exp(-1.0)), 1 / (1 + math.exp(-0.5))
+        w_first = s1 / (s1 + s05)
+    w_second = 1.0 - w_first
+    assert list(r["idx"][0]) == [2, 0]
+    np.testing.assert_allclose(r["w"][0], [w_first, w_second], rtol=1e-14)
+    y2 = _const_expert_value(X, F, *consts[2])
+    y0 = _const_expert_value(X, F, *consts[0])
+    expect = w_first * y2 + w_second * y0
+    np.testing.assert_allclose(r["y"][0], np.full(H, expect), rtol=1e-12)
+    # the pin separates the right pairing from the swapped one by far more than its tolerance
+    assert abs((w_second * y2 + w_first * y0) - expect) > 1e-3 * abs(expect)
+
+
+def test_stack_two_layers_closed_form():
+    """Two layers of one constant-code int4 expert each (k = 1, weight 1), written out by hand.
+
+    x0 = 2 s with s = +1 on the first 80 of 128 entries and -1 on the rest.  Layer 0 sees
+    xn0 = bf16(x0 / sqrt(4 + eps)) = s exactly, so X0 = 32 and y0 is the constant v0; then
+    x1 = 2 s + v0 has two distinct values a+, a-, mean square 4 + v0^2 + 2*2*v0*32/128, and
+    layer 1 sees their bf16-rounded normalised values, X1 = 80 n+ + 48 n-; y1 = v1 and
+    x2 = x1 + v1.  A wrong layer order, a dropped residual or a norm of the wrong x fails."""
+    H = F = 128
+    eps = 1e-6
+    s = np.where(np.arange(H) < 80, 1.0, -1.0)
+    c0, c1 = (3, -2, 5), (-1, 4, 7)
+    blob0 = _int4_expert_blob(H, F, *c0, SG, SU, SD)
+    blob1 = _int4_expert_blob(H, F, *c1, SG, SU, 2.0 ** -7)
+    one = np.ones((1, H), np.float32)
+    layers = [lambda xn: O.layer(xn, one, 1, O.SOFTMAX, lambda e: blob0, INT4, H, F),
+              lambda xn: O.layer(xn, one, 1, O.SOFTMAX, lambda e: blob1, INT4, H, F)]
+    x_final, res = O.stack((2.0 * s)[None, :], layers, eps=eps)
+
+    np.testing.assert_array_equal(res[0]["xn"][0], bits(s))
+    v0 = _const_expert_value(32.0, F, *c0)
+    ms1 = 4.0 + v0 * v0 + 2 * 2.0 * v0 * 32.0 / 128.0
+    n_plus = float(S.bf16_bits_to_f32(bits(np.float32((2.0 + v0) / math.sqrt(ms1 + eps)))))
+    n_minus = float(S.bf16_bits_to_f32(bits(np.float32((-2.0 + v0) / math.sqrt(ms1 + eps)))))
+    np.testing.assert_array_equal(res[1]["xn"][0], bits(np.where(s > 0, n_plus, n_minus)))
+    v1 = _const_expert_value(80 * n_plus + 48 * n_minus, F, *c1, sd=2.0 ** -7)
+    assert abs(v0) > 0.1 and abs(v1) > 0.01
+    np.testing.assert_allclose(x_final[0], 2.0 * s + v0 + v1, rtol=1e-12, atol=1e-14)

@@ -59,7 +59,7 @@ def test_route_noalloc_matches_forward(H, E, k, router, T):
     import routed_expert_ffn_03_gb300 as M
     from routed_expert_ffn_03_gb300 import build
     build.build()
-    spec = LayerSpec(H, 128, E, k, S.INT4, router=router, seed=31 + router + H + E)
+    spec = LayerSpec(H, 64, E, k, S.RVQ, router=router, seed=31 + router + H + E)
     xb = x_tokens(spec.seed, 1, T, spec.H)
     (idx_ref, w_ref), = _forward_routing(spec, [xb], T)
     _check_oracle(spec, xb, idx_ref)
@@ -80,7 +80,7 @@ def test_route_noalloc_back_to_back_on_one_stream(H, E, k, router, T):
     each call's routing lands in its own output buffers and equals moe_forward's."""
     import torch
     import routed_expert_ffn_03_gb300 as M
-    spec = LayerSpec(H, 128, E, k, S.INT4, router=router, seed=77 + H + E)
+    spec = LayerSpec(H, 64, E, k, S.RVQ, router=router, seed=77 + H + E)
     xbs = [x_tokens(spec.seed, i, T, spec.H) for i in (3, 4)]
     refs = _forward_routing(spec, xbs, T)
     W = torch.from_numpy(spec.router_w(0)).cuda()

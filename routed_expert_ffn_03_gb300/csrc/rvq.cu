@@ -90,6 +90,16 @@ __device__ __forceinline__ void rvq_half_sum(const uint4 (&v)[RV_HQ], uint32_t d
   }
 }
 
+// D += A B on tf32 operands (m16n8k8): a = (row g, col p), (g+8, p), (g, p+4), (g+8, p+4);
+// b = (row p, col g), (p+4, g).  bf16 inputs and fp16 codebook entries are exact in tf32.
+__device__ __forceinline__ void mma_1688_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 struct RvUnit {
   int pass, m, ks, expert;
   const uint8_t* base;   // matrix base (codebooks first)
@@ -175,13 +185,24 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
     uint4 ha[RV_HQ], hb[RV_HQ];
     if (ti < seg_end) load_half<0>(ha, codes + (size_t)(ti - useg) * RVQ_TASK_BYTES, lane);
 
-    // this warp's codebook fragments (6 n-tiles of 8 entries) go in flight now as well
+    // this warp's codebook fragments (6 n-tiles of 8 entries) go in flight now as well:
+    // gate/up as tf32 (elements p and p + 4 of the entry), down as fp16 pairs (2p, 2p + 1)
     constexpr int RV_NT = 96 / RV_NW;
-    uint32_t bfr[RV_NT];
+    uint32_t bfr[RV_NT], bfr1[RV_NT];
     {
       const uint32_t* cb = reinterpret_cast<const uint32_t*>(U.base);  // fp16 [768][8]
+      const __half* cbh = reinterpret_cast<const __half*>(U.base);
 #pragma unroll
-      for (int n = 0; n < RV_NT; ++n) bfr[n] = __ldg(cb + ((warp + n * RV_NW) * 8 + gq) * 4 + p);
+      for (int n = 0; n < RV_NT; ++n) {
+        const int e = (warp + n * RV_NW) * 8 + gq;
+        if (DOWN) {
+          bfr[n] = __ldg(cb + e * 4 + p);
+          bfr1[n] = 0u;
+        } else {
+          bfr[n] = __float_as_uint(__half2float(__ldg(cbh + e * 8 + p)));
+          bfr1[n] = __float_as_uint(__half2float(__ldg(cbh + e * 8 + p + 4)));
+        }
+      }
     }
 
     if (!waited) {
@@ -225,23 +246,33 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
     }
     __syncthreads();
     {
-      // A fragments: rows = groups q, k = element i (hi and lo parts)
-      uint32_t ahi[4][2], alo[4][2];
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int q = 16 * mt + gq + 8 * h;
-          __half h0, l0, h1, l1;
-          split_half(vin[q * 8 + 2 * p], h0, l0);
-          split_half(vin[q * 8 + 2 * p + 1], h1, l1);
-          ahi[mt][h] = pack_half2(h0, h1);
-          alo[mt][h] = pack_half2(l0, l1);
-        }
-      }
       int jofs[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) jofs[r] = 8 * ((p + r) & 3);
+      // A fragments: rows = groups q, k = element i.  gate/up: the bf16 input is exact in
+      // tf32, one tf32 mma per product; down: the fp32 input as fp16 hi + lo, two mma.
+      uint32_t at[4][4];
+      uint32_t ahi[4][2], alo[4][2];
+      if (!DOWN) {
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            at[mt][r] = __float_as_uint(vin[(16 * mt + gq + 8 * (r & 1)) * 8 + p + 4 * (r >> 1)]);
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int q = 16 * mt + gq + 8 * h;
+            __half h0, l0, h1, l1;
+            split_half(vin[q * 8 + 2 * p], h0, l0);
+            split_half(vin[q * 8 + 2 * p + 1], h1, l1);
+            ahi[mt][h] = pack_half2(h0, h1);
+            alo[mt][h] = pack_half2(l0, l1);
+          }
+        }
+      }
 #pragma unroll
       for (int n = 0; n < RV_NT; ++n) {
         const int e0 = (warp + n * RV_NW) * 8;
@@ -249,10 +280,15 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
 #pragma unroll
         for (int P = 0; P < 2; ++P) {
           float dA[4] = {0.f, 0.f, 0.f, 0.f}, dB[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_1688(dA, ahi[2 * P][0], ahi[2 * P][1], b);
-          mma_1688(dA, alo[2 * P][0], alo[2 * P][1], b);
-          mma_1688(dB, ahi[2 * P + 1][0], ahi[2 * P + 1][1], b);
-          mma_1688(dB, alo[2 * P + 1][0], alo[2 * P + 1][1], b);
+          if (!DOWN) {
+            mma_1688_tf32(dA, at[2 * P], b, bfr1[n]);
+            mma_1688_tf32(dB, at[2 * P + 1], b, bfr1[n]);
+          } else {
+            mma_1688(dA, ahi[2 * P][0], ahi[2 * P][1], b);
+            mma_1688(dA, alo[2 * P][0], alo[2 * P][1], b);
+            mma_1688(dB, ahi[2 * P + 1][0], ahi[2 * P + 1][1], b);
+            mma_1688(dB, alo[2 * P + 1][0], alo[2 * P + 1][1], b);
+          }
           // value j of entry e: q = 32P + g + 8j  (j: A row g, A row g+8, B row g, B row g+8).
           // Store r writes value j = (p + r) & 3, so one store touches 32 banks: the values
           // are rotated left by p with two conditional swaps instead of indexed selects.

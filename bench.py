@@ -202,6 +202,39 @@ def measure_link_gbs(device):
     return best
 
 
+def measure_record_copy_gbs(device, rec_bytes, n=48):
+    """Host -> device bandwidth of back-to-back copies of one expert record each (pinned
+    source), on one stream and spread over four: best of 3.  The link figure at the copy
+    size the streamed tier issues."""
+    import torch
+    h = torch.empty(n * rec_bytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n * rec_bytes, dtype=torch.uint8, device="cuda:%d" % device)
+    out = {}
+    for ns in (1, 4):
+        streams = [torch.cuda.Stream(device=device) for _ in range(ns)]
+        best = 0.0
+        for _ in range(3):
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(streams[0])
+            for st in streams[1:]:
+                st.wait_event(e0)
+            for i in range(n):
+                with torch.cuda.stream(streams[i % ns]):
+                    d[i * rec_bytes:(i + 1) * rec_bytes].copy_(h[i * rec_bytes:(i + 1) * rec_bytes], non_blocking=True)
+            ends = []
+            for st in streams:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(st)
+                ends.append(ev)
+            torch.cuda.synchronize()
+            ms = max(e0.elapsed_time(ev) for ev in ends)
+            best = max(best, n * rec_bytes / (ms / 1e3) / 1e9)
+        out["record_copy_gbs_%dstream%s" % (ns, "" if ns == 1 else "s")] = round(best, 2)
+    del h, d
+    return out
+
+
 def gateup_bytes_per_expert(cfg):
     H, F = cfg["H"], cfg["F"]
     if cfg["wfmt"] == S.INT4:
@@ -521,6 +554,7 @@ def run_gpu(args, cfg, rank, world, device):
     }
     if streamed:
         link = measure_link_gbs(device)
+        rec_copy = measure_record_copy_gbs(device, st["record_bytes"])
         miss_gbs = st["bytes_h2d"] / max(1e-9, st["h2d_ms"] / 1e3) / 1e9 if st["h2d_ms"] else None
         out["hit_series_per64"] = hit_series
         if args.hit_sweep and T == 1:
@@ -543,6 +577,7 @@ def run_gpu(args, cfg, rank, world, device):
                             "expert bytes copied (misses and read-ahead) / time the link was busy (union of the "
                             "copy batches)",
             "cache_slots": st["cache_slots"]}
+        out["streaming"].update(rec_copy)
         if cfg.get("pool_file"):
             out["streaming"]["file_tier"] = {
                 "file_bytes": cfg["file_bytes"], "ram_cache_bytes": int(cfg["host_cache"]),

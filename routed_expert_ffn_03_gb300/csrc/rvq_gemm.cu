@@ -12,10 +12,12 @@
 // tile), in that order; a block (8 warps) takes an equal contiguous range of items, so
 // its consecutive items share the group and k-slice and the B operand (X hi/lo, K-major
 // canonical layout, no swizzle, built from 16-byte loads) is built once for them.  Per
-// item: one bulk TMA copy each of the matrix's codebooks (12 KB) and the tile's codes
-// (4 row blocks x 6 KB); then for each of
+// item: the tile's codes (4 row blocks x 6 KB) arrive by a bulk TMA copy issued while the
+// item before was computing (two code buffers), the matrix's codebooks (12 KB) by a copy
+// only when the matrix changes; then for each of
 // the 8 k-blocks of 64 inputs the block gathers the three A stage tiles (128 x 64 fp16
-// each, K-major canonical layout) into one of two buffers and one thread issues
+// each, K-major canonical layout; a thread reads its row's 12 code bytes of 4 groups as 3
+// words) into one of two buffers and one thread issues
 // 3 x 4 tcgen05.mma (M = 128, N = 16..64, K = 16) into the TMEM accumulator, committing
 // to that buffer's mbarrier so the gather of the next k-block overlaps them.  The
 // epilogue reads TMEM with tcgen05.ld (warps 0-3, one TMEM lane quarter each) and writes
@@ -36,10 +38,10 @@ constexpr int GM_CODES = 4 * RVQ_TASK_BYTES;                // 24576 (4 row bloc
 constexpr int GM_B = GM_MAXN * RVQ_KS * RVQ_GROUP * 2;      // 65536: N x 512 fp16
 constexpr int GM_ASTAGE = GM_TILE_M * GM_KB * 2;            // 16384: 128 x 64 fp16
 constexpr int GM_A = 2 * 3 * GM_ASTAGE;                     // two buffers x three stages
-constexpr int GM_OFF_CODES = GM_CB;
-constexpr int GM_OFF_B = GM_OFF_CODES + GM_CODES;
+constexpr int GM_OFF_CODES = GM_CB;                         // two buffers: item i's codes, item i + 1's
+constexpr int GM_OFF_B = GM_OFF_CODES + 2 * GM_CODES;
 constexpr int GM_OFF_A = GM_OFF_B + GM_B;
-constexpr int GM_OFF_BAR = GM_OFF_A + GM_A;                 // 3 mbarriers + tmem address
+constexpr int GM_OFF_BAR = GM_OFF_A + GM_A;                 // 5 mbarriers + tmem address
 constexpr int GM_SMEM = GM_OFF_BAR + 64;
 constexpr int GM_THREADS = 256;
 constexpr int GM_TMEM_COLS = 64;
@@ -115,13 +117,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
   const int rows32 = g.ntask * 32, rows32_gu = gg.ntask * 32;
 
   uint8_t* cb = smem;
-  uint8_t* codes = smem + GM_OFF_CODES;
   uint8_t* bsm = smem + GM_OFF_B;
   uint8_t* asm_ = smem + GM_OFF_A;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GM_OFF_BAR);  // [0] tma, [1..2] mma buffers
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM_OFF_BAR + 32);
+  // [0] codebooks, [1..2] mma buffers, [3..4] code buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GM_OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + GM_OFF_BAR + 48);
   __shared__ volatile int s_abort;
-  const uint32_t bar_tma = smem_u32(bars), bar_mma0 = smem_u32(bars + 1);
+  const uint32_t bar_cb = smem_u32(bars), bar_mma0 = smem_u32(bars + 1), bar_code0 = smem_u32(bars + 3);
 
   const int n_big = __ldcg(&a.plan.hdr->n_big);
   const int total = n_big * mats * nks * ntile;
@@ -130,9 +132,11 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
   if (it0 >= it1) return;  // no item for this block (uniform): no tensor memory taken
 
   if (tid == 0) {
-    mbar_init(bar_tma, 1);
+    mbar_init(bar_cb, 1);
     mbar_init(bar_mma0, 1);
     mbar_init(bar_mma0 + 8, 1);
+    mbar_init(bar_code0, 1);
+    mbar_init(bar_code0 + 8, 1);
     s_abort = 0;
     mbar_fence_init();
   }
@@ -147,10 +151,13 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  int tma_phase = 0, mma_phase[2] = {0, 0}, mma_pending[2] = {0, 0};
+  int cb_phase = 0, mma_phase[2] = {0, 0}, mma_pending[2] = {0, 0};
+  int code_phase[2] = {0, 0}, code_pending[2] = {0, 0};   // thread 0's view of the code copies
+  bool cb_pending = false;
   __shared__ int s_tok[GEMM_MAX_TOKENS];
   int b_grp = -1, b_ks = -1;    // the group and k-slice the B operand holds
-  for (int it = it0; it < it1 && !s_abort; ++it) {
+  int cb_grp = -1, cb_m = -1;   // the matrix whose codebooks are in shared memory
+  auto decode = [&](int it) {
     GmItem I;
     I.tile = it % ntile;
     int rest = it / ntile;
@@ -158,22 +165,48 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
     rest /= mats;
     I.ks = rest % nks;
     I.grp = rest / nks;
+    return I;
+  };
+  auto matrix_of = [&](const GmItem& I) {
     const int expert = __ldcg(a.plan.big + 3 * I.grp + 0);
+    return expert_record(a, expert) + (DOWN ? rg.off[2] : (I.m == 0 ? rg.off[0] : rg.off[1]));
+  };
+  // thread 0: the codes of item `it` (4 row blocks of its tile, one k-slice) into buffer b
+  auto issue_codes = [&](int it, int b) {
+    const GmItem I = decode(it);
+    const int rb0 = I.tile * 4, nrb = min(4, g.ntask - rb0);
+    const uint8_t* mat = matrix_of(I);
+    fence_async_smem();  // an earlier item read this buffer through the generic proxy
+    mbar_arrive_expect_tx(bar_code0 + 8 * b, nrb * RVQ_TASK_BYTES);
+    bulk_g2s(smem_u32(smem + GM_OFF_CODES + b * GM_CODES), mat + GM_CB + ((size_t)I.ks * g.ntask + rb0) * RVQ_TASK_BYTES,
+             nrb * RVQ_TASK_BYTES, bar_code0 + 8 * b);
+    code_pending[b] = 1;
+  };
+  if (tid == 0) issue_codes(it0, 0);
+  for (int it = it0; it < it1 && !s_abort; ++it) {
+    const int cur = (it - it0) & 1;
+    const GmItem I = decode(it);
     const int pass0 = __ldcg(a.plan.big + 3 * I.grp + 1);
     const int ntok = __ldcg(a.plan.big + 3 * I.grp + 2);
     const int N = max(16, (2 * ntok + 15) & ~15);
-    const uint8_t* mat = expert_record(a, expert) + (DOWN ? rg.off[2] : (I.m == 0 ? rg.off[0] : rg.off[1]));
+    const uint8_t* mat = matrix_of(I);
     const int rb0 = I.tile * 4, nrb = min(4, g.ntask - rb0);
+    const uint8_t* codes = smem + GM_OFF_CODES + cur * GM_CODES;
 
-    // codebooks and codes of this tile and slice
     if (tid == 0) {
-      const uint32_t bytes = GM_CB + nrb * RVQ_TASK_BYTES;
-      fence_async_smem();  // the previous item read these buffers through the generic proxy
-      mbar_arrive_expect_tx(bar_tma, bytes);
-      bulk_g2s(smem_u32(cb), mat, GM_CB, bar_tma);
-      bulk_g2s(smem_u32(codes), mat + GM_CB + ((size_t)I.ks * g.ntask + rb0) * RVQ_TASK_BYTES,
-               nrb * RVQ_TASK_BYTES, bar_tma);
+      // the next item's codes go in flight now (its buffer was last read by the item before)
+      if (it + 1 < it1) issue_codes(it + 1, cur ^ 1);
+      // codebooks only when the matrix changes (the previous item's gathers are done)
+      if (I.grp != cb_grp || I.m != cb_m) {
+        fence_async_smem();
+        mbar_arrive_expect_tx(bar_cb, GM_CB);
+        bulk_g2s(smem_u32(cb), mat, GM_CB, bar_cb);
+        cb_pending = true;
+      }
     }
+    const bool new_cb = I.grp != cb_grp || I.m != cb_m;
+    cb_grp = I.grp;
+    cb_m = I.m;
     // B operand: column n = 2 t + part of token t of the group, K-major canonical layout;
     // one thread step = 8 consecutive inputs of one token (hi and lo columns)
     if (I.grp != b_grp || I.ks != b_ks) {
@@ -230,9 +263,15 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
       b_grp = I.grp;
       b_ks = I.ks;
     }
-    // the tile's codes must have landed before the gather
-    bool ok = mbar_wait_bounded(bar_tma, tma_phase & 1, a.budget);
-    tma_phase ^= 1;
+    // the tile's codes (and new codebooks) must have landed before the gather
+    bool ok = mbar_wait_bounded(bar_code0 + 8 * cur, code_phase[cur] & 1, a.budget);
+    code_phase[cur] ^= 1;
+    if (tid == 0 && ok) code_pending[cur] = 0;
+    if (ok && new_cb) {
+      ok = mbar_wait_bounded(bar_cb, cb_phase & 1, a.budget);
+      cb_phase ^= 1;
+      if (tid == 0 && ok) cb_pending = false;
+    }
     if (!ok) {
       s_abort = 1;
       atomicOr(a.status, ST_TIMEOUT);
@@ -254,20 +293,34 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
         }
         tc_fence_after();
       }
-      // gather: (row, group of 8 inputs, stage) -> 16 B codebook row into stage tile
-      for (int e = tid; e < GM_TILE_M * 8; e += GM_THREADS) {
-        const int r = e & (GM_TILE_M - 1), gi = e >> 7;  // gi: group within the k-block
+      // gather: thread = (tile row r, 4 groups of the k-block); the 4 groups' 12 code bytes
+      // are 12 contiguous bytes of the row's lane stream (positions P .. P + 3, P = (l ^ q) & ~3
+      // for its first group q), read as 3 words; each (position, stage) gives one 16-byte
+      // codebook row, stored into the stage tile at the row's group q = l ^ position
+      {
+        const int r = tid & (GM_TILE_M - 1), hh = tid >> 7;   // GM_THREADS == 2 * GM_TILE_M
         const int rbl = r >> 5, l = r & 31;
-        const int q = kb * 8 + gi;                        // group within the slice
-        const int i = l ^ q;                              // position in the lane stream
-        const uint8_t* lanebase = codes + rbl * RVQ_TASK_BYTES + l * 16;
+        const int q0 = kb * 8 + 4 * hh;                        // first group (within the slice)
+        const int P = (l ^ q0) & ~3;                           // first position of the 4
+        uint32_t w[3] = {0u, 0u, 0u};
+        if (rbl < nrb) {
+          const uint8_t* lb = codes + rbl * RVQ_TASK_BYTES + l * 16;
 #pragma unroll
-        for (int s = 0; s < 3; ++s) {
-          const int bp = 3 * i + s;                       // stream byte
-          uint32_t code = 0;
-          if (rbl < nrb) code = lanebase[(bp >> 4) * 512 + (bp & 15)];
-          const uint4 v = *reinterpret_cast<const uint4*>(cb + ((s * 256 + code) * 8) * 2);
-          *reinterpret_cast<uint4*>(abuf + s * GM_ASTAGE + canon_off(r, gi * 8, GM_KB / 8)) = v;
+          for (int j = 0; j < 3; ++j) {
+            const int bp = 3 * P + 4 * j;                      // stream byte, 4-aligned
+            w[j] = *reinterpret_cast<const uint32_t*>(lb + (bp >> 4) * 512 + (bp & 15));
+          }
+        }
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+          const int gi = ((P + d) ^ l) - kb * 8;               // group within the k-block
+#pragma unroll
+          for (int s = 0; s < 3; ++s) {
+            const int b = 3 * d + s;                           // byte of the 12
+            const uint32_t code = (w[b >> 2] >> (8 * (b & 3))) & 0xffu;
+            const uint4 v = *reinterpret_cast<const uint4*>(cb + ((s * 256 + code) * 8) * 2);
+            *reinterpret_cast<uint4*>(abuf + s * GM_ASTAGE + canon_off(r, gi * 8, GM_KB / 8)) = v;
+          }
         }
       }
       fence_async_smem();
@@ -336,6 +389,11 @@ __global__ void __launch_bounds__(GM_THREADS, 1) rvq_gemm_kernel(ExpertArgs a) {
     for (int b = 0; b < 2; ++b)
       if (mma_pending[b] && !mbar_wait_bounded(bar_mma0 + 8 * b, mma_phase[b] & 1, a.budget))
         atomicOr(a.status, ST_TIMEOUT);
+    // bulk copies this block started and nobody waited for (a time-out, or the last prefetch)
+    for (int b = 0; b < 2; ++b)
+      if (code_pending[b] && !mbar_wait_bounded(bar_code0 + 8 * b, code_phase[b] & 1, a.budget))
+        atomicOr(a.status, ST_TIMEOUT);
+    if (cb_pending && !mbar_wait_bounded(bar_cb, cb_phase & 1, a.budget)) atomicOr(a.status, ST_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();

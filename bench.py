@@ -423,11 +423,14 @@ def run_gpu(args, cfg, rank, world, device):
         x.copy_(x0_dev[0])
         layers()
     torch.cuda.synchronize()
+    launches_per_step = None
     if not streamed:
+        before = ctx.stats()["launches"]
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             layers()
         torch.cuda.synchronize()
+        launches_per_step = ctx.stats()["launches"] - before   # the kernels of one replay
 
     def step(i):
         x.copy_(x0_dev[i % n_inp])
@@ -548,7 +551,7 @@ def run_gpu(args, cfg, rank, world, device):
         "expert_gbs": round(expert_gbs, 1), "hbm_frac": round(expert_gbs / peak, 4),
         "hit_rate": round(st["hits"] / max(1, st["lookups"]), 4),
         "roofline": roofline, "e2e": e2e,
-        "gpu_launches": K * (L * 4 + 1),
+        "gpu_launches": K * launches_per_step if launches_per_step is not None else st["launches"],
         "clocks": clk,
         "wall_s": round(wall, 3),
     }

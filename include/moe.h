@@ -133,6 +133,9 @@ typedef struct {
     unsigned long long ram_misses;            /* HBM misses read from the file first (pool_file) */
     double file_read_ms;                      /* wall time of the file read batches */
     int file_direct;                          /* 1 when the file is read with O_DIRECT */
+    unsigned long long launches;              /* kernels launched by the forward calls (counted on
+                                                 the host when the call queues them; calls recorded
+                                                 into a CUDA graph count once, at capture) */
 } moe_stats_t;
 
 typedef struct moe_ctx moe_ctx;

@@ -166,6 +166,7 @@ struct moe_ctx {
   uint8_t* d_rec_stage = nullptr;
 
   unsigned long long hits = 0, misses = 0, bytes_h2d = 0;
+  unsigned long long launches = 0;  // kernels this context launched for forwards (host-side count)
   double h2d_ms = 0.0;
   int fail_copies = 0;
   moe_status sticky = MOE_OK;
@@ -855,6 +856,7 @@ static moe_status readahead(moe_ctx* c, int nl, const void* x, int T) {
   ra.record_bytes = 0;
   ra.big_min = 0;
   CK(launch_router(ra, c->num_sms, c->pred));
+  ++c->launches;
   CK(cudaMemcpyAsync(c->h_rb2, c->plan2.hdr, 4 * sizeof(int), cudaMemcpyDeviceToHost, c->pred));
   CK(cudaMemcpyAsync(c->h_rb2 + 8, c->plan2.uniq, (size_t)E * sizeof(int), cudaMemcpyDeviceToHost, c->pred));
   CK(cudaStreamSynchronize(c->pred));
@@ -929,6 +931,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   ra.big_min = c->big_min;
   if (c->prof && !c->streamed) CK(cudaEventRecordWithFlags(c->prof_ev[(size_t)layer * 5], s, cudaEventRecordExternal));
   CK(launch_router(ra, c->num_sms, s));
+  ++c->launches;
 
   CombineArgs ca{};
   ca.plan = c->plan;
@@ -956,6 +959,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
       CK(launch_int4_gateup(a, c->num_sms, s));
       if (ev) CK(cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal));
       CK(launch_int4_down(a, c->num_sms, s));
+      c->launches += 2;
     } else if (c->big_min > 0) {
       // per-token path over the small passes, tcgen05 path over the dense groups
       ExpertArgs as = a;
@@ -965,14 +969,17 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
       CK(launch_rvq_gemm_gateup(a, c->num_sms, s));
       if (ev) CK(cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal));
       CK(launch_rvq_down(as, c->num_sms, s));
-      CK(launch_rvq_gemm_down(a, c->num_sms, s, c->max_big));
+      CK(launch_rvq_gemm_down(a, c->num_sms, s, c->max_big));   // SwiGLU of the dense groups, then their down
+      c->launches += 5;
     } else {
       CK(launch_rvq_gateup(a, c->num_sms, s));
       if (ev) CK(cudaEventRecordWithFlags(ev[2], s, cudaEventRecordExternal));
       CK(launch_rvq_down(a, c->num_sms, s));
+      c->launches += 2;
     }
     if (ev) CK(cudaEventRecordWithFlags(ev[3], s, cudaEventRecordExternal));
     CK(launch_combine(ca, s));
+    ++c->launches;
     if (ev) {
       CK(cudaEventRecordWithFlags(ev[4], s, cudaEventRecordExternal));
       c->prof_seen[layer] = 1;
@@ -1064,6 +1071,7 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     a.range.p_begin = 0;
     a.range.p_end = n_first;
     CK(launch_experts(c, a, s));
+    c->launches += 2;
   }
 
   // miss copies on the side streams (round-robin), in ascending expert id, one event each
@@ -1125,8 +1133,10 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     a.range.p_begin = group_begin[m];
     a.range.p_end = group_begin[m + 1];
     CK(launch_experts(c, a, s));
+    c->launches += 2;
   }
   CK(launch_combine(ca, s));
+  ++c->launches;
   c->last_T[layer] = T;
   if (c->readahead && layer + 1 < c->cfg.num_layers && layer_ready(c, layer + 1) == MOE_OK)
     return readahead(c, layer + 1, x, T);
@@ -1158,6 +1168,7 @@ moe_status moe_forward_residual(moe_ctx* c, int layer, float* x, const float* y_
   if ((size_t)T * c->cfg.hidden <= 32768 && T <= ROUTER_FUSED_MAXT)
     return forward_impl(c, layer, nullptr, x, y_prev, xn, eps, y, T, s);
   CK(launch_residual_rmsnorm(x, y_prev, xn, T, c->cfg.hidden, eps, s));
+  ++c->launches;
   return forward_impl(c, layer, xn, nullptr, nullptr, nullptr, 0.f, y, T, s);
 }
 
@@ -1183,6 +1194,7 @@ moe_status moe_residual_rmsnorm(moe_ctx* c, float* x, const float* y, uint16_t* 
   if (c->sticky != MOE_OK) return c->sticky;
   DeviceGuard dg(c->device);
   CK(launch_residual_rmsnorm(x, y, xn, T, c->cfg.hidden, eps, (cudaStream_t)stream));
+  ++c->launches;
   return MOE_OK;
 }
 
@@ -1215,6 +1227,7 @@ moe_status moe_stats(moe_ctx* c, moe_stats_t* out) {
     out->file_read_ms = c->ft->read_ms;
     out->file_direct = c->ft->direct() ? 1 : 0;
   }
+  out->launches = c->launches;
   return st;
 }
 
@@ -1227,6 +1240,7 @@ moe_status moe_reset_stats(moe_ctx* c) {
   if (c->streamed) batch_drain(c, true);
   c->hits = c->misses = c->bytes_h2d = 0;
   c->prefetches = c->prefetch_hits = 0;
+  c->launches = 0;
   c->h2d_ms = 0.0;
   if (c->ft) {
     c->ft->reads = c->ft->read_bytes = c->ft->ram_hits = c->ft->ram_misses = 0;

@@ -48,7 +48,7 @@ class Stats(ctypes.Structure):
         "bytes_router", "bytes_h2d", "record_bytes", "cache_slots")] + [("h2d_ms", ctypes.c_double)] + [
         (n, ctypes.c_ulonglong) for n in ("prefetches", "prefetch_hits", "file_reads", "file_read_bytes",
                                           "ram_hits", "ram_misses")] + [
-        ("file_read_ms", ctypes.c_double), ("file_direct", ctypes.c_int)]
+        ("file_read_ms", ctypes.c_double), ("file_direct", ctypes.c_int), ("launches", ctypes.c_ulonglong)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -349,3 +349,28 @@ def test_engine_lru_matches_the_host_replay():
         rate = bench.lru_hit_rate(trace, slots, SPEC.k)
         assert st["lookups"] == sum(len(set(r[0])) for r in routes)
         assert st["hits"] == round(rate * st["lookups"])
+
+
+def test_launch_count_in_stats():
+    """moe_stats counts the kernels the forward calls queue: router, gate/up, down and
+    combine per layer (7 when the dense path serves experts with many tokens), one per
+    residual RMS norm."""
+    import torch
+    spec = LayerSpec(256, 128, 8, 2, S.RVQ, router=0, seed=41)
+    for T, per_forward in ((1, 4), (16, 7)):
+        ctx = make_context(spec, T)
+        try:
+            ctx.reset_stats()
+            xb = x_tokens(41, 0, T, spec.H)
+            x = torch.from_numpy(xb.view(np.int16).copy()).cuda()
+            out = torch.empty((T, spec.H), dtype=torch.float32, device="cuda")
+            ctx.forward(0, x, out, T)
+            xr = torch.zeros((T, spec.H), dtype=torch.float32, device="cuda")
+            xn = torch.zeros((T, spec.H), dtype=torch.int16, device="cuda")
+            ctx.residual_rmsnorm(xr, out, xn, T)
+            torch.cuda.synchronize()
+            assert ctx.stats()["launches"] == per_forward + 1
+            ctx.reset_stats()
+            assert ctx.stats()["launches"] == 0
+        finally:
+            ctx.close()

@@ -173,7 +173,11 @@ size_t moe_expert_blob_bytes(int wfmt, int hidden, int ffn);
  * graph.  Streamed mode: blocks the host once per call to read the routing back, then
  * issues the miss copies on a side stream, hits first, each missed expert's kernels
  * waiting for its own copy.  Errors: MOE_EINVAL (T outside 1..max_tokens, layer out of
- * range, null pointers), MOE_ESTATE (layer not fully registered), sticky errors. */
+ * range, null pointers), MOE_ESTATE (layer not fully registered), sticky errors.
+ * Numerics: the int4 kernels, and the RVQ down projection, carry their activations as fp16
+ * hi + lo pairs (their sum equals the fp32 value to 2^-22 of it), so the input x and the
+ * SwiGLU activations silu(W_g x) * (W_u x) must stay below 65504 in magnitude; sums are
+ * fp32 and the output is fp32. */
 moe_status moe_forward(moe_ctx* ctx, int layer, const void* x_bf16, float* out, int T, void* stream);
 
 /* One layer of the residual stack, fused:  if y_prev != NULL: x += y_prev;

@@ -77,3 +77,44 @@ def test_device_generator_matches_host():
         D.make_expert_blob_device(5, 2, 3, wfmt, H, F, dev)
         torch.cuda.synchronize()
         np.testing.assert_array_equal(dev.cpu().numpy(), host)
+
+
+def _int4_wide_scale_blob(spec, layer, e, rng):
+    """The generator's int4 blob of expert e with every fp16 group scale replaced by a
+    random positive value over 20 binades: subnormal (2^-24 and up) to 2^-4, plus zeros.
+    The activations stay far inside fp16's range (the kernels carry them as fp16 hi + lo)."""
+    blob = spec.blob(layer, e).copy()
+    off = 0
+    for rows, K in S.matrix_shapes(spec.H, spec.F):
+        nb = rows * K // 2
+        ns = rows * (K // S.INT4_GROUP)
+        expo = rng.integers(0, 12, ns).astype(np.uint16)          # 0 = subnormal, 11 = 2^-4
+        mant = rng.integers(0, 1024, ns).astype(np.uint16)
+        bits = (expo << 10) | mant
+        bits[rng.random(ns) < 0.02] = 0                           # some zero scales
+        blob[off + nb:off + nb + 2 * ns] = bits.view(np.uint8)
+        off += nb + 2 * ns
+    assert off == blob.size
+    return blob
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_int4_scales_over_the_fp16_range(T):
+    """int4 group scales from fp16 subnormals to 2^-4 (the generator's own scales sit in
+    [2^-8, 2^-7)): every group's sum is scaled by its own fp16 value on the GPU as in the
+    oracle."""
+    import routed_expert_ffn_03_gb300 as M
+    spec = LayerSpec(512, 384, 6, 2, S.INT4, router=0, seed=91)
+    rng = np.random.default_rng(91)
+    blobs = {e: _int4_wide_scale_blob(spec, 0, e, rng) for e in range(spec.E)}
+    ctx = M.Context(1, spec.H, spec.F, spec.E, spec.k, spec.wfmt, router=spec.router, max_tokens=T)
+    try:
+        ctx.register_router(0, spec.router_w(0))
+        for e in range(spec.E):
+            ctx.register_expert(0, e, blobs[e])
+        xb = x_tokens(spec.seed, 5, T, spec.H)
+        y, idx, w = gpu_forward(ctx, 0, xb)
+        r = compare(oracle_forward(spec, 0, xb, dict(blobs)), y, idx, w)
+        assert r["rms"] > 0
+    finally:
+        ctx.close()

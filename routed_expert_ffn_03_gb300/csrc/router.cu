@@ -48,6 +48,48 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Pieces shared by the three router kernels, so that each gives the same bits:
+// the W slice of a warp's expert (RSW inputs from h0, 8 float4 per lane, loaded before the
+// dependency wait), the bf16 rounding of four normalised inputs, and a warp's dot product
+// of its W slice with a staged bf16 slice of x (per-lane fma chain in input order, then
+// the warp tree).
+__device__ __forceinline__ void router_w_slice(const RouterArgs& a, int e, bool live, int h0, int lane,
+                                               float4 (&wv)[RSW / 128]) {
+  const float* wr = a.W + (size_t)(live ? e : 0) * a.H;
+#pragma unroll
+  for (int i = 0; i < RSW / 128; ++i) {
+    const int h = h0 + 4 * (lane + 32 * i);
+    wv[i] = (live && h < a.H) ? __ldg(reinterpret_cast<const float4*>(wr + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+__device__ __forceinline__ uint2 bf16x4_scaled(const float4 v, float inv) {
+  uint2 o;
+  o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x * inv)) |
+        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y * inv)) << 16);
+  o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z * inv)) |
+        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w * inv)) << 16);
+  return o;
+}
+
+// xs: the slice's bf16 inputs (element j of the slice at xs[j]); with CHECK, elements at
+// or past lim are zero (not read)
+template <bool CHECK>
+__device__ __forceinline__ float slice_dot(const float4 (&wv)[RSW / 128], const uint16_t* xs, int lane, int lim) {
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < RSW / 128; ++i) {
+    const int j = 4 * (lane + 32 * i);
+    uint2 xb = make_uint2(0u, 0u);
+    if (!CHECK || j < lim) xb = *reinterpret_cast<const uint2*>(xs + j);
+    acc = fmaf(wv[i].x, __uint_as_float(xb.x << 16), acc);
+    acc = fmaf(wv[i].y, __uint_as_float(xb.x & 0xffff0000u), acc);
+    acc = fmaf(wv[i].z, __uint_as_float(xb.y << 16), acc);
+    acc = fmaf(wv[i].w, __uint_as_float(xb.y & 0xffff0000u), acc);
+  }
+  return warp_sum(acc);
+}
+
 // dense-group split of an expert's c tokens (pmax == 1): chunks of <= GEMM_MAX_TOKENS
 __device__ __forceinline__ int big_chunks(int c, int big_min) {
   return (big_min > 0 && c >= big_min) ? cdiv(c, GEMM_MAX_TOKENS) : 0;
@@ -418,14 +460,7 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
 
   // ---------------- W slice of this warp's expert (independent of the kernel before)
   float4 wv[RSW / 128];
-  {
-    const float* wr = a.W + (size_t)(live ? e : 0) * a.H;
-#pragma unroll
-    for (int i = 0; i < RSW / 128; ++i) {
-      const int h = h0 + 4 * (lane + 32 * i);
-      wv[i] = (live && h < a.H) ? __ldg(reinterpret_cast<const float4*>(wr + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
+  router_w_slice(a, e, live, h0, lane, wv);
 
   pdl_wait();  // x (and the residual) come from the kernels before
   pdl_launch_dependents();
@@ -458,12 +493,7 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
 #pragma unroll
     for (int t = 0; t < ROUTER_FUSED_MAXT; ++t) {
       if (t < a.T && threadIdx.x < RSW / 4) {
-        const float inv = s_inv[t];
-        uint2 v;
-        v.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].x * inv)) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].y * inv)) << 16);
-        v.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].z * inv)) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].w * inv)) << 16);
+        uint2 v = bf16x4_scaled(xv[t], s_inv[t]);
         if (!in) v = make_uint2(0u, 0u);
         *reinterpret_cast<uint2*>(xs + t * RSW + hq) = v;
         if (g == 0 && in) *reinterpret_cast<uint2*>(a.xn_out + (size_t)t * a.H + h) = v;
@@ -487,17 +517,7 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
     if (live) {
       float keep = 0.f;
       for (int tl = 0; tl < nt; ++tl) {
-        const uint16_t* xr = xs + tl * RSW;
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < RSW / 128; ++i) {
-          const uint2 xb = *reinterpret_cast<const uint2*>(xr + 4 * (lane + 32 * i));
-          acc = fmaf(wv[i].x, __uint_as_float(xb.x << 16), acc);
-          acc = fmaf(wv[i].y, __uint_as_float(xb.x & 0xffff0000u), acc);
-          acc = fmaf(wv[i].z, __uint_as_float(xb.y << 16), acc);
-          acc = fmaf(wv[i].w, __uint_as_float(xb.y & 0xffff0000u), acc);
-        }
-        acc = warp_sum(acc);
+        const float acc = slice_dot<false>(wv, xs + tl * RSW, lane, RSW);
         if (lane == tl) keep = acc;
       }
       if (lane < nt) a.partial[((size_t)sl * a.T + tg + lane) * a.E + e] = keep;
@@ -579,14 +599,7 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
   const int T = a.T, H = a.H;
 
   float4 wv[RSW / 128];
-  {
-    const float* wr = a.W + (size_t)(live ? e : 0) * H;
-#pragma unroll
-    for (int i = 0; i < RSW / 128; ++i) {
-      const int h = h0 + 4 * (lane + 32 * i);
-      wv[i] = (live && h < H) ? __ldg(reinterpret_cast<const float4*>(wr + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
+  router_w_slice(a, e, live, h0, lane, wv);
 
   pdl_wait();  // x (and the residual) come from the kernels before
   pdl_launch_dependents();
@@ -654,12 +667,7 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
 #pragma unroll
     for (int t = 0; t < ROUTER_FUSED_MAXT; ++t) {
       if (t < T && threadIdx.x < RSW / 4) {
-        const float inv = s_inv[t];
-        uint2 v;
-        v.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].x * inv)) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].y * inv)) << 16);
-        v.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].z * inv)) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(xv[t].w * inv)) << 16);
+        uint2 v = bf16x4_scaled(xv[t], s_inv[t]);
         if (!in) v = make_uint2(0u, 0u);
         *reinterpret_cast<uint2*>(xs + t * RSW + hq) = v;
         if (g == 0 && in) *reinterpret_cast<uint2*>(a.xn_out + (size_t)t * H + h) = v;
@@ -685,17 +693,7 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
     if (live) {
       float keep = 0.f;
       for (int tl = 0; tl < nt; ++tl) {
-        const uint16_t* xr = xs + tl * RSW;
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < RSW / 128; ++i) {
-          const uint2 xb = *reinterpret_cast<const uint2*>(xr + 4 * (lane + 32 * i));
-          acc = fmaf(wv[i].x, __uint_as_float(xb.x << 16), acc);
-          acc = fmaf(wv[i].y, __uint_as_float(xb.x & 0xffff0000u), acc);
-          acc = fmaf(wv[i].z, __uint_as_float(xb.y << 16), acc);
-          acc = fmaf(wv[i].w, __uint_as_float(xb.y & 0xffff0000u), acc);
-        }
-        acc = warp_sum(acc);
+        const float acc = slice_dot<false>(wv, xs + tl * RSW, lane, RSW);
         if (lane == tl) keep = acc;
       }
       if (lane < nt) part0[(tg + lane) * REPB + warp] = keep;
@@ -783,14 +781,7 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
   int* s_pos = s_idx + T * k;                                            // [T*k]
 
   float4 wv[RSW / 128];
-  {
-    const float* wr = a.W + (size_t)(live ? e : 0) * H;
-#pragma unroll
-    for (int i = 0; i < RSW / 128; ++i) {
-      const int h = h0 + 4 * (lane + 32 * i);
-      wv[i] = (live && h < H) ? __ldg(reinterpret_cast<const float4*>(wr + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
+  router_w_slice(a, e, live, h0, lane, wv);
   pdl_wait();  // x (and the residual) come from the kernels before
   pdl_launch_dependents();
   if (fused && H <= RMS_NTHR * V4 * 4) {
@@ -817,11 +808,7 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
       for (int q = 0; q < V4; ++q) {
         const int i = threadIdx.x + q * RMS_NTHR;
         if ((int)threadIdx.x < RMS_NTHR && i < H / 4) {
-          uint2 o;
-          o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[q].x * inv)) |
-                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[q].y * inv)) << 16);
-          o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[q].z * inv)) |
-                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[q].w * inv)) << 16);
+          const uint2 o = bf16x4_scaled(v[q], inv);
           *reinterpret_cast<uint2*>(a.xn_out + ro + 4 * i) = o;
           *reinterpret_cast<uint2*>(xs + ro + 4 * i) = o;
         }
@@ -846,11 +833,7 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
           const float4 y4 = __ldcg(reinterpret_cast<const float4*>(a.yprev + o));
           x4.x += y4.x; x4.y += y4.y; x4.z += y4.z; x4.w += y4.w;
         }
-        const float inv = s_inv[t];
-        v.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.x * inv)) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.y * inv)) << 16);
-        v.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.z * inv)) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x4.w * inv)) << 16);
+        v = bf16x4_scaled(x4, s_inv[t]);
         *reinterpret_cast<uint2*>(a.xn_out + o) = v;
       } else {
         v = __ldg(reinterpret_cast<const uint2*>(a.x + o));
@@ -863,19 +846,7 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
   if (live) {
     float keep = 0.f;
     for (int t = 0; t < T; ++t) {
-      const uint16_t* xr = xs + (size_t)t * H;
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < RSW / 128; ++i) {
-        const int h = h0 + 4 * (lane + 32 * i);
-        uint2 xb = make_uint2(0u, 0u);
-        if (h < H) xb = *reinterpret_cast<const uint2*>(xr + h);
-        acc = fmaf(wv[i].x, __uint_as_float(xb.x << 16), acc);
-        acc = fmaf(wv[i].y, __uint_as_float(xb.x & 0xffff0000u), acc);
-        acc = fmaf(wv[i].z, __uint_as_float(xb.y << 16), acc);
-        acc = fmaf(wv[i].w, __uint_as_float(xb.y & 0xffff0000u), acc);
-      }
-      acc = warp_sum(acc);
+      const float acc = slice_dot<true>(wv, xs + (size_t)t * H + h0, lane, H - h0);
       if (lane == t) keep = acc;
     }
     if (lane < T) spart[((size_t)lane * E + e) * NS + sl] = keep;

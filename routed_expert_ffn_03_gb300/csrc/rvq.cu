@@ -101,8 +101,8 @@ __device__ __forceinline__ void mma_1688_tf32(float (&d)[4], const uint32_t (&a)
 }
 
 struct RvUnit {
-  int pass, m, ks, expert;
-  const uint8_t* base;   // matrix base (codebooks first)
+  int pass, m, ks, expert, tok;   // tok: the pass's token (gate/up; one token per pass)
+  const uint8_t* base;            // matrix base (codebooks first)
 };
 
 template <bool DOWN>
@@ -115,6 +115,7 @@ __device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, i
   const int pi = pm / mats;
   U.pass = a.range.order ? __ldcg(a.range.order + p_begin + pi) : p_begin + pi;
   U.expert = __ldcg(a.plan.pass_expert + U.pass);
+  U.tok = DOWN ? 0 : __ldcg(a.plan.pass_tok + U.pass);
   U.base = expert_record(a, U.expert) + (DOWN ? rg.off[2] : (U.m == 0 ? rg.off[0] : rg.off[1]));
   return U;
 }
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
     pdl_wait();
     pdl_launch_dependents();
   }
+  static_assert(RVQ_KS * RVQ_GROUP == RV_NW * 32, "one input element of a k-slice per thread");
   for (int i = t0; i < t1;) {
     const int u = i / ntask;
     const int seg_end = min(t1, (u + 1) * ntask);
@@ -210,16 +212,21 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
       pdl_launch_dependents();
       waited = true;
     }
+    // gate/up: this thread's input element of the k-slice goes in flight with the rest
+    float xv = 0.f;
+    if (!DOWN) {
+      const int k = U.ks * RVQ_KS * RVQ_GROUP + (int)threadIdx.x;   // one element per thread
+      if (k < g.K) xv = bf16_bits_to_float(a.x[(size_t)U.tok * a.H + k]);
+    }
     __syncthreads();  // the previous unit's table is no longer read
     {
-      const int tok = __ldcg(a.plan.pass_tok + U.pass);   // one token per pass
       const int kbase = U.ks * RVQ_KS * RVQ_GROUP;
       for (int e = threadIdx.x; e < RVQ_KS * RVQ_GROUP; e += nthr) {
         const int k = kbase + e;
         float v = 0.f;
         if (k < g.K) {
           if (!DOWN) {
-            v = bf16_bits_to_float(a.x[(size_t)tok * a.H + k]);
+            v = xv;
           } else {
             const float* pg = a.part_gu + ((size_t)(U.pass * 2 + 0) * gg.nks) * rows32_gu + k;
             const float* pu = a.part_gu + ((size_t)(U.pass * 2 + 1) * gg.nks) * rows32_gu + k;

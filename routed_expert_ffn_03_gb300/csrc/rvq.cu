@@ -231,16 +231,16 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
             const float* pg = a.part_gu + ((size_t)(U.pass * 2 + 0) * gg.nks) * rows32_gu + k;
             const float* pu = a.part_gu + ((size_t)(U.pass * 2 + 1) * gg.nks) * rows32_gu + k;
             float gs = 0.f, us = 0.f;
-            for (int s0 = 0; s0 < gg.nks; s0 += 8) {  // 16 loads in flight, added in slice order
-              float gv[8], uv[8];
+            for (int s0 = 0; s0 < gg.nks; s0 += 16) {  // 32 loads in flight, added in slice order
+              float gv[16], uv[16];
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
+              for (int q = 0; q < 16; ++q) {
                 const bool in = s0 + q < gg.nks;
                 gv[q] = in ? __ldcg(pg + (size_t)(s0 + q) * rows32_gu) : 0.f;
                 uv[q] = in ? __ldcg(pu + (size_t)(s0 + q) * rows32_gu) : 0.f;
               }
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
+              for (int q = 0; q < 16; ++q) {
                 gs += gv[q];
                 us += uv[q];
               }

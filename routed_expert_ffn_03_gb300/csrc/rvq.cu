@@ -11,8 +11,9 @@
 // which equals sum_k W[r][k] x[k] for W[r][8q+i] = C0[c0][i] + C1[c1][i] + C2[c2][i].
 //
 // Table build: D[q][e] = X[q][.] . Cb[e][.] is a [64 x 8] x [8 x 768] product done with
-// m16n8k8 tensor-core mma (the fp16 codebook entries are used as stored; the fp32 input
-// is split into fp16 hi + lo, two mma into one fp32 accumulator).  Each lane then writes
+// m16n8k8 tensor-core mma into fp32 accumulators.  gate/up: the bf16 input and the fp16
+// codebook entries are exact in tf32, one tf32 mma per product.  down: the fp32 SwiGLU
+// input is split into fp16 hi + lo, two fp16 mma into one accumulator.  Each lane then writes
 // its accumulators in a rotated order so that one store instruction touches 32 banks.
 //
 // Lookups: lane l owns row 32*block + l and visits the 64 groups in the order
@@ -120,6 +121,81 @@ __device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, i
   return U;
 }
 
+// Cost of one segment (a unit's table build plus the block's start on it) in tasks of
+// 32 rows: a block that touches one more unit with the same number of tasks finishes
+// about 3.5 us later, the time of 22 tasks.
+constexpr int RV_SEG_COST = 22;
+
+// Greedy advance inside units of n tasks: from task u * n + r (r < n), spend a budget B
+// (a segment costs RV_SEG_COST plus its tasks) without passing unit u_end.  No division:
+// in the regime it serves a budget spans at most three units.
+__device__ __forceinline__ void rv_advance(int& u, int& r, int B, int u_end, int n) {
+  constexpr int C = RV_SEG_COST;
+  while (u < u_end && B > C) {
+    const int take = min(n - r, B - C);
+    B -= C + take;
+    r += take;
+    if (r == n) {
+      ++u;
+      r = 0;
+    }
+  }
+}
+
+// Split u_n units of n tasks over G < u_n < 2 G blocks for the least maximum cost, where
+// a block's cost is its tasks plus RV_SEG_COST for each unit it touches.  Candidates:
+// equal task ranges, and for g = 1..8 groups of g blocks (the last group holds the G mod
+// g left over) in which every block spends at most a budget M, every full group holding
+// the same number of whole units.  Lane j of each warp evaluates one candidate; the warp
+// takes the least budget (ties to the lower lane).  Every block computes the same split.
+__device__ __forceinline__ void rv_split(int u_n, int n, int G, int b, int lane, int& t0, int& t1) {
+  constexpr int C = RV_SEG_COST;
+  const int W = n + C;                          // cost of a whole unit
+  const int total = u_n * n;
+  int M = 1 << 26;
+  const int g = lane + 1;
+  const int ng = G / g, rem = G - ng * g;
+  int cg = 0;
+  if (lane < 8 && ng > 0) {
+    const int k = (u_n * g + G - 1) / G;
+    for (int kk = max(1, k - 1); kk <= k + 1; ++kk) {
+      const int Mk = (kk * W + C * (g - 1) + g - 1) / g;
+      const int capr = rem ? max(0, (rem * Mk - C * (rem - 1)) / W) : 0;
+      if (ng * kk + capr >= u_n) {
+        M = Mk;
+        cg = kk;
+        break;
+      }
+    }
+  } else if (lane == 8) {
+    const int L = (total + G - 1) / G;
+    M = L + C * ((L + n - 2) / n + 1);
+  }
+  const unsigned key = (unsigned)min(M, (1 << 26) - 1) << 5 | (unsigned)lane;
+  const unsigned best = __reduce_min_sync(0xffffffffu, key);
+  const int wl = best & 31;
+  if (wl == 8) {
+    t0 = (int)((long long)total * b / G);
+    t1 = (int)((long long)total * (b + 1) / G);
+    return;
+  }
+  const int Mb = (int)(best >> 5);
+  const int gb = wl + 1, ngb = G / gb;
+  const int cgb = __shfl_sync(0xffffffffu, cg, wl);
+  const int j = b / gb, i = b - j * gb, gj = j < ngb ? gb : G - ngb * gb;
+  const int u0 = min(u_n, j * cgb);
+  const int u1 = j < ngb ? min(u_n, u0 + cgb) : u_n;
+  int u = u0, r = 0;
+  for (int ii = 0; ii < i; ++ii) rv_advance(u, r, Mb, u1, n);
+  t0 = u * n + r;
+  if (i == gj - 1) {
+    t1 = u1 * n;
+  } else {
+    rv_advance(u, r, Mb, u1, n);
+    t1 = u * n + r;
+  }
+}
+
 template <bool DOWN>
 __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -151,7 +227,8 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   // Work split.  Every unit (pass, matrix, k-slice) costs a table build, so with no more
   // units than blocks each unit goes to its own group of blocks, which split its tasks:
   // every block builds one table; with at least two units per block, blocks take whole
-  // units (contiguous unit ranges); in between, equal contiguous task ranges.
+  // units (contiguous unit ranges); in between, rv_split balances the blocks' costs
+  // (tasks plus RV_SEG_COST per unit touched).
   int t0, t1;
   if (n_units >= 2 * (int)gridDim.x) {
     t0 = (int)((long long)n_units * blockIdx.x / gridDim.x) * ntask;
@@ -163,9 +240,10 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
     const int i = blockIdx.x - b_lo, n = b_hi - b_lo;
     t0 = u * ntask + (int)((long long)ntask * i / n);
     t1 = u * ntask + (int)((long long)ntask * (i + 1) / n);
+  } else if (n_units > 0) {
+    rv_split(n_units, ntask, gridDim.x, blockIdx.x, lane, t0, t1);
   } else {
-    t0 = (int)((long long)total * blockIdx.x / gridDim.x);
-    t1 = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+    t0 = t1 = 0;
   }
   const uint32_t l4 = (uint32_t)lane << 2;
   const uint32_t delta = smem_u32(smem) - RV_DYN_BASE;   // 0 on the fast path

@@ -121,77 +121,109 @@ __device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, i
   return U;
 }
 
-// Cost of one segment (a unit's table build plus the block's start on it) in tasks of
-// 32 rows: a block that touches one more unit with the same number of tasks finishes
-// about 3.5 us later, the time of 22 tasks.
-constexpr int RV_SEG_COST = 22;
+// Block split cost model, fitted to per-warp timestamps of the gate/up kernel: a warp's
+// task takes ~2.3 us and warps take the tasks of a unit in rounds of RV_NW, so a block
+// pays one round (RV_RND_COST) per started round of each unit it touches, plus ~2.0 us
+// (RV_SEG_COST) per unit for the table build and the unit's start.
+constexpr int RV_RND_COST = 8;
+constexpr int RV_SEG_COST = 7;
 
-// Greedy advance inside units of n tasks: from task u * n + r (r < n), spend a budget B
-// (a segment costs RV_SEG_COST plus its tasks) without passing unit u_end.  No division:
-// in the regime it serves a budget spans at most three units.
-__device__ __forceinline__ void rv_advance(int& u, int& r, int B, int u_end, int n) {
-  constexpr int C = RV_SEG_COST;
-  while (u < u_end && B > C) {
-    const int take = min(n - r, B - C);
-    B -= C + take;
-    r += take;
-    if (r == n) {
+// Split of u_n units over the grid: groups of g blocks, every full group holding kk whole
+// units and spending at most m_full per block; the G mod g blocks left over form the last
+// group, which holds the rest of the units at most m_rem per block.
+struct RvSplit {
+  int g, kk, m_full, m_rem;
+};
+
+// Greedy advance: from task u * n + r (r a multiple of RV_NW), take whole rounds of unit
+// u, then of the next units, while the budget B pays a segment and a round; stops at
+// unit u_end.  nr = rounds per unit.  Returns the budget spent.
+__device__ __forceinline__ int rv_advance(int& u, int& r, int B, int u_end, int nr) {
+  const int B0 = B;
+  while (u < u_end && B >= RV_SEG_COST + RV_RND_COST) {
+    const int left = nr - r / RV_NW;
+    const int take = min((B - RV_SEG_COST) / RV_RND_COST, left);
+    B -= RV_SEG_COST + RV_RND_COST * take;
+    if (take == left) {
       ++u;
       r = 0;
+    } else {
+      r += RV_NW * take;
     }
   }
+  return B0 - B;
 }
 
-// Split u_n units of n tasks over G < u_n < 2 G blocks for the least maximum cost, where
-// a block's cost is its tasks plus RV_SEG_COST for each unit it touches.  Candidates:
-// equal task ranges, and for g = 1..8 groups of g blocks (the last group holds the G mod
-// g left over) in which every block spends at most a budget M, every full group holding
-// the same number of whole units.  Lane j of each warp evaluates one candidate; the warp
-// takes the least budget (ties to the lower lane).  Every block computes the same split.
-__device__ __forceinline__ void rv_split(int u_n, int n, int G, int b, int lane, int& t0, int& t1) {
-  constexpr int C = RV_SEG_COST;
-  const int W = n + C;                          // cost of a whole unit
-  const int total = u_n * n;
-  int M = 1 << 26;
-  const int g = lane + 1;
-  const int ng = G / g, rem = G - ng * g;
-  int cg = 0;
-  if (lane < 8 && ng > 0) {
-    const int k = (u_n * g + G - 1) / G;
-    for (int kk = max(1, k - 1); kk <= k + 1; ++kk) {
-      const int Mk = (kk * W + C * (g - 1) + g - 1) / g;
-      const int capr = rem ? max(0, (rem * Mk - C * (rem - 1)) / W) : 0;
-      if (ng * kk + capr >= u_n) {
-        M = Mk;
-        cg = kk;
-        break;
-      }
+// cost of the tasks from u * n + r to the end of unit u_end - 1
+__device__ __forceinline__ int rv_tail_cost(int u, int r, int u_end, int nr) {
+  if (u >= u_end) return 0;
+  int c = 0;
+  if (r > 0) {
+    c = RV_SEG_COST + RV_RND_COST * (nr - r / RV_NW);
+    ++u;
+  }
+  return c + (u_end - u) * (RV_SEG_COST + RV_RND_COST * nr);
+}
+
+// `units` whole units over gg blocks: the budget per block (x) and the largest block cost
+// (y) of the greedy split, whose last block takes what is left
+__device__ __forceinline__ int2 rv_group(int units, int gg, int nr) {
+  const int W = RV_SEG_COST + RV_RND_COST * nr;
+  const int M0 = (units * W + RV_SEG_COST * (gg - 1) + gg - 1) / gg;
+  int u = 0, r = 0, mx = 0;
+  for (int i = 0; i < gg - 1; ++i) mx = max(mx, rv_advance(u, r, M0, units, nr));
+  return make_int2(M0, max(mx, rv_tail_cost(u, r, units, nr)));
+}
+
+// The split of u_n units of n tasks over G blocks (G < u_n < 2 G) with the least largest
+// block cost among groups of g = 1..8 blocks and kk = ceil(u_n g / G) - 1 + {0, 1, 2}
+// units per full group: lane 3 (g - 1) + j of the warp evaluates one candidate, the warp
+// takes the cheapest (ties to the lower lane).  Every warp of every block computes the
+// same split.  g = 1, kk = ceil(u_n / G) is always valid.
+__device__ __forceinline__ RvSplit rv_plan(int u_n, int n, int G, int lane) {
+  const int nr = (n + RV_NW - 1) / RV_NW;
+  int cost = (1 << 26) - 1;
+  RvSplit sp{1, 0, 0, 0};
+  if (lane < 24) {
+    const int g = lane / 3 + 1, ng = G / g, rem = G - ng * g;
+    const int kk = (u_n * g + G - 1) / G - 1 + lane % 3;
+    const int ur = max(0, u_n - ng * kk);
+    if (ng > 0 && kk >= 1 && (ur == 0 || rem > 0)) {
+      const int2 f = rv_group(min(kk, u_n), g, nr);
+      const int2 rr = ur > 0 ? rv_group(ur, rem, nr) : make_int2(0, 0);
+      cost = min(max(f.y, rr.y), (1 << 26) - 1);
+      sp = RvSplit{g, kk, f.x, rr.x};
     }
-  } else if (lane == 8) {
-    const int L = (total + G - 1) / G;
-    M = L + C * ((L + n - 2) / n + 1);
   }
-  const unsigned key = (unsigned)min(M, (1 << 26) - 1) << 5 | (unsigned)lane;
-  const unsigned best = __reduce_min_sync(0xffffffffu, key);
+  const unsigned best = __reduce_min_sync(0xffffffffu, (unsigned)cost << 5 | (unsigned)lane);
   const int wl = best & 31;
-  if (wl == 8) {
-    t0 = (int)((long long)total * b / G);
-    t1 = (int)((long long)total * (b + 1) / G);
-    return;
+  return RvSplit{__shfl_sync(0xffffffffu, sp.g, wl), __shfl_sync(0xffffffffu, sp.kk, wl),
+                 __shfl_sync(0xffffffffu, sp.m_full, wl), __shfl_sync(0xffffffffu, sp.m_rem, wl)};
+}
+
+// block b's task range [t0, t1) under the split sp
+__device__ __forceinline__ void rv_range(const RvSplit& sp, int u_n, int n, int G, int b, int& t0, int& t1) {
+  const int nr = (n + RV_NW - 1) / RV_NW;
+  const int ng = G / sp.g, j = b / sp.g, i = b - j * sp.g;
+  int u0, u1, B, gj;
+  if (j < ng) {
+    u0 = min(u_n, j * sp.kk);
+    u1 = min(u_n, u0 + sp.kk);
+    B = sp.m_full;
+    gj = sp.g;
+  } else {
+    u0 = min(u_n, ng * sp.kk);
+    u1 = u_n;
+    B = sp.m_rem;
+    gj = G - ng * sp.g;
   }
-  const int Mb = (int)(best >> 5);
-  const int gb = wl + 1, ngb = G / gb;
-  const int cgb = __shfl_sync(0xffffffffu, cg, wl);
-  const int j = b / gb, i = b - j * gb, gj = j < ngb ? gb : G - ngb * gb;
-  const int u0 = min(u_n, j * cgb);
-  const int u1 = j < ngb ? min(u_n, u0 + cgb) : u_n;
   int u = u0, r = 0;
-  for (int ii = 0; ii < i; ++ii) rv_advance(u, r, Mb, u1, n);
+  for (int ii = 0; ii < i; ++ii) rv_advance(u, r, B, u1, nr);
   t0 = u * n + r;
   if (i == gj - 1) {
     t1 = u1 * n;
   } else {
-    rv_advance(u, r, Mb, u1, n);
+    rv_advance(u, r, B, u1, nr);
     t1 = u * n + r;
   }
 }
@@ -215,35 +247,42 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   // older than the gate/up kernel (that kernel waited for it before letting this one
   // start), and the weights before it waits, so its first codes and codebooks are in
   // flight while gate/up finishes; the gate/up partials are read after the wait.
+  const int G = gridDim.x;
+  const int p_begin = a.range.p_begin;
+  // Work split.  Every unit (pass, matrix, k-slice) costs a table build, so with no more
+  // units than blocks each unit goes to its own group of blocks, which split its tasks:
+  // every block builds one table; with at least two units per block, blocks take whole
+  // units (contiguous unit ranges); in between, rv_plan balances the blocks' costs.  In
+  // gate/up a pass count fixed at launch (one token) gives that balanced split before the
+  // wait, while the kernel before still runs (down waits later anyway).
+  int t0 = 0, t1 = -1;   // t1 < 0: not split yet
+  if (!DOWN && a.range.p_end >= 0) {
+    const int u_n = max(0, a.range.p_end - p_begin) * mats * nks;
+    if (u_n > G && u_n < 2 * G) rv_range(rv_plan(u_n, ntask, G, lane), u_n, ntask, G, blockIdx.x, t0, t1);
+  }
   if (!DOWN) {
     pdl_wait();
     pdl_launch_dependents();
   }
   bool waited = !DOWN;
-  const int p_begin = a.range.p_begin;
-  const int p_end = a.range.p_end >= 0 ? a.range.p_end : __ldcg(a.range.count ? a.range.count : &a.plan.hdr->n_pass);
-  const int n_units = max(0, p_end - p_begin) * mats * nks;
-  const int total = n_units * ntask;
-  // Work split.  Every unit (pass, matrix, k-slice) costs a table build, so with no more
-  // units than blocks each unit goes to its own group of blocks, which split its tasks:
-  // every block builds one table; with at least two units per block, blocks take whole
-  // units (contiguous unit ranges); in between, rv_split balances the blocks' costs
-  // (tasks plus RV_SEG_COST per unit touched).
-  int t0, t1;
-  if (n_units >= 2 * (int)gridDim.x) {
-    t0 = (int)((long long)n_units * blockIdx.x / gridDim.x) * ntask;
-    t1 = (int)((long long)n_units * (blockIdx.x + 1) / gridDim.x) * ntask;
-  } else if (n_units > 0 && n_units <= (int)gridDim.x) {
-    const int u = (int)((long long)blockIdx.x * n_units / gridDim.x);
-    const int b_lo = (int)(((long long)u * gridDim.x + n_units - 1) / n_units);
-    const int b_hi = (int)(((long long)(u + 1) * gridDim.x + n_units - 1) / n_units);
-    const int i = blockIdx.x - b_lo, n = b_hi - b_lo;
-    t0 = u * ntask + (int)((long long)ntask * i / n);
-    t1 = u * ntask + (int)((long long)ntask * (i + 1) / n);
-  } else if (n_units > 0) {
-    rv_split(n_units, ntask, gridDim.x, blockIdx.x, lane, t0, t1);
-  } else {
-    t0 = t1 = 0;
+  if (t1 < 0) {
+    const int p_end = a.range.p_end >= 0 ? a.range.p_end : __ldcg(a.range.count ? a.range.count : &a.plan.hdr->n_pass);
+    const int n_units = max(0, p_end - p_begin) * mats * nks;
+    if (n_units >= 2 * G) {
+      t0 = (int)((long long)n_units * blockIdx.x / G) * ntask;
+      t1 = (int)((long long)n_units * (blockIdx.x + 1) / G) * ntask;
+    } else if (n_units > 0 && n_units <= G) {
+      const int u = (int)((long long)blockIdx.x * n_units / G);
+      const int b_lo = (int)(((long long)u * G + n_units - 1) / n_units);
+      const int b_hi = (int)(((long long)(u + 1) * G + n_units - 1) / n_units);
+      const int i = blockIdx.x - b_lo, n = b_hi - b_lo;
+      t0 = u * ntask + (int)((long long)ntask * i / n);
+      t1 = u * ntask + (int)((long long)ntask * (i + 1) / n);
+    } else if (n_units > 0) {
+      rv_range(rv_plan(n_units, ntask, G, lane), n_units, ntask, G, blockIdx.x, t0, t1);
+    } else {
+      t1 = 0;
+    }
   }
   const uint32_t l4 = (uint32_t)lane << 2;
   const uint32_t delta = smem_u32(smem) - RV_DYN_BASE;   // 0 on the fast path

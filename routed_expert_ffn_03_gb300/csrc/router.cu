@@ -39,8 +39,6 @@ constexpr int REPB = 8;     // experts per block (one per warp)
 constexpr int RTG = 32;     // tokens staged per pass over the slice
 int router_nch(int H) { return cdiv(H, RSW) + 1; }     // slices of partials + the logits
 int router_tickets(int E) { return cdiv(E, REPB) + 1; }
-constexpr int RCAND = 64;   // candidates of a token ranked exactly (more: iterative selection)
-constexpr int RCAND_WARP = RCAND + 32;   // (logit, id) pairs per warp: candidates + the k selected
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -98,110 +96,55 @@ __device__ __forceinline__ int big_chunks(int c, int big_min) {
 // Top-k of one token's E logits (one warp; NV * 32 >= E values, lane l holds experts
 // l + 32 i), then the k weights; writes the plan's and the per-layer copy of the routing.
 // Order: logits descending, equal logits by ascending id; NaN ranks as -inf.
-// The k-th largest of the 32 lane maxima (maxima of distinct experts) is a lower bound tau
-// of the k-th largest logit, so the top k are among the experts with logit >= tau; when
-// those candidates are at most RCAND (the usual case: about 1.5 k) each one's rank among
-// them is counted directly.  Otherwise (many equal logits) the warp selects the best k
-// one after the other: each lane keeps the maximum of its experts not yet taken, the warp
-// takes the best, and only the lane that gave it away looks for its next one.
-// cand: this warp's RCAND_WARP pairs of shared memory.
+// Selection by k warp reductions: each lane keeps the best of its experts not yet taken
+// as an order-preserving 32-bit key of the logit (-0 taken as +0) and its id; the warp's
+// largest key, then the least id holding it, is the next expert, and only the lane that
+// owned it looks for its next best.
+__device__ __forceinline__ uint32_t logit_key(float x) {
+  const uint32_t b = __float_as_uint(x + 0.0f);   // -0 + 0 = +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 template <int NV>
 __device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src, bool global_src, int t, int lane,
-                                           int* s_idx, float2* cand) {
+                                           int* s_idx) {
   const int E = a.E, k = a.k;
-  float v[NV];
-  float m = -INFINITY;
+  uint32_t key[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int ee = lane + 32 * i;
     const float x = ee < E ? (global_src ? __ldcg(src + ee) : src[ee]) : -INFINITY;
-    v[i] = x != x ? -INFINITY : x;
-    m = fmaxf(m, v[i]);
+    key[i] = ee < E ? logit_key(x != x ? -INFINITY : x) : 0u;   // 0: below every expert's key
   }
-  // With E <= RCAND every expert is a candidate, in place (candidate e = expert e).
-  // Otherwise tau = the k-th largest lane maximum (lane order breaks ties: the ranks are
-  // distinct), and the candidates are packed by a warp scan.
-  int C = E, inc = 0, c = 0;
-  uint32_t cm = 0u;
-  if (E > RCAND) {
-    int r = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float o = __shfl_sync(0xffffffffu, m, j);
-      r += (o > m || (o == m && j < lane)) ? 1 : 0;
-    }
-    const float tau = __shfl_sync(0xffffffffu, m, __ffs(__ballot_sync(0xffffffffu, r == k - 1)) - 1);
+  uint32_t taken = 0u;
+  uint32_t lk;
+  int le;
+  auto lane_best = [&]() {
+    lk = 0u;
+    le = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-      if (lane + 32 * i < E && v[i] >= tau) { cm |= 1u << i; ++c; }
-    inc = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += y;
-    }
-    C = __shfl_sync(0xffffffffu, inc, 31);
-  }
+      if (!((taken >> i) & 1u) && key[i] > lk) {   // ascending ids: the first of equal keys stays
+        lk = key[i];
+        le = lane + 32 * i;
+      }
+  };
+  lane_best();
   int my_e = 0;
   float my_l = 0.f;
-  if (C <= RCAND) {
-    float2* sel = cand + RCAND;
-    if (E <= RCAND) {
-#pragma unroll
-      for (int i = 0; i < NV; ++i)
-        if (lane + 32 * i < E) cand[lane + 32 * i] = make_float2(v[i], __int_as_float(lane + 32 * i));
-    } else {
-      int pos = inc - c;
-#pragma unroll
-      for (int i = 0; i < NV; ++i)
-        if ((cm >> i) & 1u) cand[pos++] = make_float2(v[i], __int_as_float(lane + 32 * i));
+  for (int j = 0; j < k; ++j) {
+    const uint32_t bk = __reduce_max_sync(0xffffffffu, lk);
+    const int be = (int)__reduce_min_sync(0xffffffffu, lk == bk ? (uint32_t)le : 0xffffffffu);
+    if (lane == j) {
+      my_e = be;
+      my_l = key_logit(bk);
     }
-    __syncwarp();
-    for (int q = lane; q < C; q += 32) {
-      const float2 me = cand[q];
-      const int mid = __float_as_int(me.y);
-      int rk = 0;
-#pragma unroll 8
-      for (int j = 0; j < C; ++j) {
-        const float2 o = cand[j];
-        rk += (o.x > me.x || (o.x == me.x && __float_as_int(o.y) < mid)) ? 1 : 0;
-      }
-      if (rk < k) sel[rk] = me;
-    }
-    __syncwarp();
-    if (lane < k) {
-      my_l = sel[lane].x;
-      my_e = __float_as_int(sel[lane].y);
-    }
-    __syncwarp();   // the buffers are this warp's next token's
-  } else {
-    uint32_t taken = 0u;
-    auto lane_best = [&](float& bv, int& be) {
-      bv = -INFINITY;
-      be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int ee = lane + 32 * i;
-        if (ee < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && ee < be))) { bv = v[i]; be = ee; }
-      }
-    };
-    float lv;
-    int le;
-    lane_best(lv, le);
-    for (int j = 0; j < k; ++j) {
-      float bv = lv;
-      int be = le;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      if (lane == j) { my_e = be; my_l = bv; }
-      if (be == le) {   // this lane's maximum was taken (ids are distinct across lanes)
-        taken |= 1u << ((be - lane) >> 5);
-        lane_best(lv, le);
-      }
+    if (le == be) {   // this lane's best was taken (ids are distinct across lanes)
+      taken |= 1u << ((be - lane) >> 5);
+      lane_best();
     }
   }
   // weights over the k selected (rank order = lane order)
@@ -227,22 +170,21 @@ __device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src
 // Phase 2 of the router, in one block: top-k per token from the logits lsrc [T][E]
 // (global memory when global_src), the weights, and the bucketing of the (token, rank)
 // pairs into passes.  s_cnt must be zero and the logits complete (after a barrier);
-// s_cand holds RCAND_WARP pairs per warp.  SMALL: E <= 128 (one top-k variant).
+// SMALL: E <= 128 (one top-k variant).
 template <bool SMALL>
 __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* lsrc, bool global_src, int* s_cnt,
-                                              int* s_off, int* s_idx, int* s_pos, int* s_routed, float2* s_cand) {
+                                              int* s_off, int* s_idx, int* s_pos, int* s_routed) {
   __shared__ int s_wsum[64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int E = a.E, T = a.T, k = a.k, pmax = a.pmax;
-  float2* cand = s_cand + (size_t)warp * RCAND_WARP;
   if (T == 1 && a.big_min != 1) {
     // one token, in warp 0 alone: every selected expert has one pass, the passes in
     // ascending expert id, the shared expert's last; no expert reaches a dense group
     if (warp != 0) return;
-    if (SMALL || E <= 128) topk_token<4>(a, lsrc, global_src, 0, lane, s_idx, cand);
-    else if (E <= 256) topk_token<8>(a, lsrc, global_src, 0, lane, s_idx, cand);
-    else if (E <= 512) topk_token<16>(a, lsrc, global_src, 0, lane, s_idx, cand);
-    else topk_token<32>(a, lsrc, global_src, 0, lane, s_idx, cand);
+    if (SMALL || E <= 128) topk_token<4>(a, lsrc, global_src, 0, lane, s_idx);
+    else if (E <= 256) topk_token<8>(a, lsrc, global_src, 0, lane, s_idx);
+    else if (E <= 512) topk_token<16>(a, lsrc, global_src, 0, lane, s_idx);
+    else topk_token<32>(a, lsrc, global_src, 0, lane, s_idx);
     __syncwarp();
     const int ee = lane < k ? s_idx[lane] : 0x7fffffff;
     int p = 0;   // rank of the expert among the k by id (the k ids are distinct)
@@ -285,10 +227,10 @@ __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* 
   // ---------------- phase 2a: top-k per token (one warp per token)
   for (int t = warp; t < T; t += nwarps) {
     const float* src = lsrc + (size_t)t * E;
-    if (SMALL || E <= 128) topk_token<4>(a, src, global_src, t, lane, s_idx, cand);
-    else if (E <= 256) topk_token<8>(a, src, global_src, t, lane, s_idx, cand);
-    else if (E <= 512) topk_token<16>(a, src, global_src, t, lane, s_idx, cand);
-    else topk_token<32>(a, src, global_src, t, lane, s_idx, cand);
+    if (SMALL || E <= 128) topk_token<4>(a, src, global_src, t, lane, s_idx);
+    else if (E <= 256) topk_token<8>(a, src, global_src, t, lane, s_idx);
+    else if (E <= 512) topk_token<16>(a, src, global_src, t, lane, s_idx);
+    else topk_token<32>(a, src, global_src, t, lane, s_idx);
   }
   __syncthreads();
 
@@ -434,11 +376,9 @@ __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* 
   }
 }
 
-// 4-byte word of the dynamic shared memory where phase 2's candidate pairs start (after
-// s_cnt, s_off, s_idx and s_pos; 8-byte aligned)
-__host__ __device__ __forceinline__ size_t router_cand_word(int E, int T, int k) {
-  const size_t w = (size_t)2 * E + (size_t)2 * T * k;
-  return (w + 1) & ~(size_t)1;
+// bytes of phase 2's shared arrays (s_cnt, s_off, s_idx, s_pos)
+__host__ __device__ __forceinline__ size_t router_phase2_bytes(int E, int T, int k) {
+  return ((size_t)2 * E + (size_t)2 * T * k) * 4;
 }
 
 // H > 8 slices.  MINB = blocks per SM the registers must allow: 3 where the grid is
@@ -555,11 +495,10 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
   int* s_off = s_cnt + E;           // [E]
   int* s_idx = s_off + E;           // [T*k]
   int* s_pos = s_idx + T * k;       // [T*k]
-  float2* s_cand = reinterpret_cast<float2*>(sm + router_cand_word(E, T, k));
   for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
   __syncthreads();
 
-  router_finish<false>(a, logits, true, s_cnt, s_off, s_idx, s_pos, &s_routed, s_cand);
+  router_finish<false>(a, logits, true, s_cnt, s_off, s_idx, s_pos, &s_routed);
 }
 
 
@@ -725,18 +664,16 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
   int* s_off = s_cnt + E;           // [E]
   int* s_idx = s_off + E;           // [T*k]
   int* s_pos = s_idx + T * k;       // [T*k]
-  float2* s_cand = reinterpret_cast<float2*>(sm + router_cand_word(E, T, k));
   if (T != 1 || a.big_min == 1) {   // the per-expert counts (not used by the one-token plan)
     for (int q = threadIdx.x; q < E; q += blockDim.x) s_cnt[q] = 0;
     __syncthreads();
   }
-  router_finish<false>(a, logits, true, s_cnt, s_off, s_idx, s_pos, &s_routed, s_cand);
+  router_finish<false>(a, logits, true, s_cnt, s_off, s_idx, s_pos, &s_routed);
 }
 
 size_t router_cluster_smem(int H, int T, int E, int k) {
   const size_t p1 = (size_t)std::min(T, RTG) * RSW * 2 + (size_t)cdiv(H, RSW) * T * REPB * sizeof(float);
-  const size_t p2 = router_cand_word(E, T, k) * 4 + (size_t)(256 / 32) * RCAND_WARP * sizeof(float2);
-  return std::max(p1, p2);
+  return std::max(p1, router_phase2_bytes(E, T, k));
 }
 
 // ---------------------------------------------------------------- small problems, one block
@@ -750,13 +687,9 @@ constexpr int ROUTER_SMEM_MAX = 160 * 1024;
 __host__ __device__ __forceinline__ bool router_small_fits(int H, int T, int E) {
   return E * cdiv(H, RSW) <= RSMALL_THREADS / 32 && T * H <= 32768 && T <= 32;
 }
-// 4-byte word where router_small_kernel's candidate pairs start (8-byte aligned)
-__host__ __device__ __forceinline__ size_t router_small_cand_word(int H, int T, int E, int k) {
-  const size_t w = (size_t)T * H / 2 + (size_t)T * E * cdiv(H, RSW) + (size_t)T * E + (size_t)2 * E + (size_t)2 * T * k;
-  return (w + 1) & ~(size_t)1;
-}
+// bf16 inputs, slice partials, logits and phase 2's arrays
 size_t router_small_smem(int H, int T, int E, int k) {
-  return router_small_cand_word(H, T, E, k) * 4 + (size_t)(RSMALL_THREADS / 32) * RCAND_WARP * sizeof(float2);
+  return ((size_t)T * H / 2 + (size_t)T * E * cdiv(H, RSW) + (size_t)T * E + (size_t)2 * E + (size_t)2 * T * k) * 4;
 }
 
 // V4: float4s of a row each norm thread holds in registers (H <= 4 * RMS_NTHR * V4)
@@ -858,8 +791,7 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
     slog[q] = v;
   }
   __syncthreads();
-  router_finish<true>(a, slog, false, s_cnt, s_off, s_idx, s_pos, &s_routed,
-                reinterpret_cast<float2*>(sm + router_small_cand_word(H, T, E, k)));
+  router_finish<true>(a, slog, false, s_cnt, s_off, s_idx, s_pos, &s_routed);
 }
 
 cudaError_t router_set_attributes() {
@@ -879,8 +811,7 @@ cudaError_t router_set_attributes() {
 // staging of min(T, RTG) bf16 rows of a slice, then (last block) the phase-2 arrays
 size_t router_smem_bytes(int H, int T, int E, int k) {
   (void)H;
-  const size_t p2 = router_cand_word(E, T, k) * 4 + (size_t)(256 / 32) * RCAND_WARP * sizeof(float2);
-  return std::max((size_t)std::min(T, RTG) * RSW * 2, p2);
+  return std::max((size_t)std::min(T, RTG) * RSW * 2, router_phase2_bytes(E, T, k));
 }
 
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s) {

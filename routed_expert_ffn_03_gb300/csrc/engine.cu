@@ -929,6 +929,10 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   ra.counters = c->d_counters;
   ra.record_bytes = c->rec_bytes;
   ra.big_min = c->big_min;
+  // One resident RVQ token: the router writes the logits only and the two RVQ kernels
+  // take the top-k themselves (one kernel boundary and the router's last-block step fewer
+  // on the way to the first expert lookup).
+  ra.defer = (!c->streamed && c->cfg.wfmt == MOE_W_RVQ3_G8 && T == 1 && c->big_min == 0 && k <= 32 && E <= 512) ? 1 : 0;
   if (c->prof && !c->streamed) CK(cudaEventRecordWithFlags(c->prof_ev[(size_t)layer * 5], s, cudaEventRecordExternal));
   CK(launch_router(ra, c->num_sms, s));
   ++c->launches;
@@ -953,6 +957,12 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
     // one token: exactly one pass per selected expert (+ the shared one), known here, so
     // the expert kernels need not read the count from the plan
     if (T == 1 && c->big_min == 0) a.range.p_end = k + c->has_shared;
+    if (ra.defer) {
+      a.route_logits = c->d_rpart + (size_t)(router_nch(H) - 1) * E;   // after the slice partials (T = 1)
+      a.route_kind = c->cfg.router;
+      a.route = OneTokenPlan{E, k, c->pmax, c->has_shared, c->big_min, ra.store_idx, ra.store_w, c->d_counters,
+                             (unsigned long long)c->rec_bytes, (unsigned long long)E * H * 4ull};
+    }
     cudaEvent_t* ev = c->prof ? &c->prof_ev[(size_t)layer * 5] : nullptr;
     if (ev) CK(cudaEventRecordWithFlags(ev[1], s, cudaEventRecordExternal));
     if (c->cfg.wfmt == MOE_W_INT4_G128) {

@@ -37,6 +37,7 @@ struct RouterArgs {
   DevCounters* counters;
   unsigned long long record_bytes;
   int big_min;           // > 0: experts with >= big_min tokens form dense groups (pmax must be 1)
+  int defer;             // one token: write the logits only, the expert kernels route (see ExpertArgs)
 };
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s);
 cudaError_t router_set_attributes();
@@ -49,6 +50,22 @@ struct PassRange {
   const int* order;
   int p_begin, p_end;
   const int* count;   // with p_end < 0: the pass count lives here (null: the plan's n_pass)
+};
+
+// What the one-token plan needs besides the plan's own arrays.
+struct OneTokenPlan {
+  int E, k, pmax, has_shared, big_min;
+  int* store_idx;               // per-layer copy of the routing [k]
+  float* store_w;
+  DevCounters* counters;
+  unsigned long long record_bytes, router_bytes;
+};
+
+// Work split of the RVQ lookup kernel for a pass count fixed at launch, made on the host
+// (g = 0: none; the kernel splits).  Groups of g blocks, full groups holding kk units at
+// most m_full per block, the left-over blocks the rest at most m_rem per block.
+struct BlockSplit {
+  int g, kk, m_full, m_rem;
 };
 
 struct ExpertArgs {
@@ -64,6 +81,13 @@ struct ExpertArgs {
   PassRange range;
   uint32_t* status;
   unsigned long long budget;
+  // One token routed inside the RVQ kernels (the router deferred, writing the logits
+  // only): every block takes the top-k of route_logits itself, and gate/up block 0 writes
+  // the plan.  Null: the router wrote the plan.
+  const float* route_logits;
+  int route_kind;
+  OneTokenPlan route;
+  BlockSplit split;                 // set by the RVQ launchers
 };
 #ifdef __CUDACC__
 // Record of expert e (E = the shared expert): resident records sit at a fixed stride, so

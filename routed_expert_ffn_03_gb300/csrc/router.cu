@@ -24,13 +24,16 @@
 // token, straight from the logits) and the bucketing of the (token, rank) pairs by
 // expert into "passes" of up to pmax tokens: routed experts in ascending id, tokens
 // ascending, then the shared expert.  Problems that fit one block use
-// router_small_kernel, with no global partials at all.
+// router_small_kernel, with no global partials at all.  Deferred (one token): the
+// kernels stop once the logits [E] are in global memory (after the slice partials) and
+// the expert kernels take the top-k themselves (route.cuh).
 #include <cfloat>
 
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "route.cuh"
 
 namespace moe {
 
@@ -93,78 +96,30 @@ __device__ __forceinline__ int big_chunks(int c, int big_min) {
   return (big_min > 0 && c >= big_min) ? cdiv(c, GEMM_MAX_TOKENS) : 0;
 }
 
-// Top-k of one token's E logits (one warp; NV * 32 >= E values, lane l holds experts
-// l + 32 i), then the k weights; writes the plan's and the per-layer copy of the routing.
-// Order: logits descending, equal logits by ascending id; NaN ranks as -inf.
-// Selection by k warp reductions: each lane keeps the best of its experts not yet taken
-// as an order-preserving 32-bit key of the logit (-0 taken as +0) and its id; the warp's
-// largest key, then the least id holding it, is the next expert, and only the lane that
-// owned it looks for its next best.
-__device__ __forceinline__ uint32_t logit_key(float x) {
-  const uint32_t b = __float_as_uint(x + 0.0f);   // -0 + 0 = +0
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_logit(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-template <int NV>
+// Top-k of token t's E logits by one warp (route.cuh), then the k weights; writes the
+// plan's and the per-layer copy of the routing and the token's experts in s_idx.  SMALL:
+// E <= 128.
+template <bool SMALL>
 __device__ __forceinline__ void topk_token(const RouterArgs& a, const float* src, bool global_src, int t, int lane,
                                            int* s_idx) {
-  const int E = a.E, k = a.k;
-  uint32_t key[NV];
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int ee = lane + 32 * i;
-    const float x = ee < E ? (global_src ? __ldcg(src + ee) : src[ee]) : -INFINITY;
-    key[i] = ee < E ? logit_key(x != x ? -INFINITY : x) : 0u;   // 0: below every expert's key
-  }
-  uint32_t taken = 0u;
-  uint32_t lk;
-  int le;
-  auto lane_best = [&]() {
-    lk = 0u;
-    le = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (!((taken >> i) & 1u) && key[i] > lk) {   // ascending ids: the first of equal keys stays
-        lk = key[i];
-        le = lane + 32 * i;
-      }
-  };
-  lane_best();
-  int my_e = 0;
-  float my_l = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const uint32_t bk = __reduce_max_sync(0xffffffffu, lk);
-    const int be = (int)__reduce_min_sync(0xffffffffu, lk == bk ? (uint32_t)le : 0xffffffffu);
-    if (lane == j) {
-      my_e = be;
-      my_l = key_logit(bk);
-    }
-    if (le == be) {   // this lane's best was taken (ids are distinct across lanes)
-      taken |= 1u << ((be - lane) >> 5);
-      lane_best();
-    }
-  }
-  // weights over the k selected (rank order = lane order)
-  const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-  float num = 0.f;
+  const int k = a.k;
+  int my_e;
+  float my_l;
+  if (SMALL) warp_topk<4>(src, global_src, a.E, k, lane, my_e, my_l);
+  else warp_topk_any(src, global_src, a.E, k, lane, my_e, my_l);
+  const float w = route_weight(a.kind, k, lane, my_l);
   if (lane < k) {
-    if (a.kind == 0) num = expf(my_l - lmax);
-    else num = 1.f / (1.f + expf(-my_l));
-  }
-  float den = num;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  if (lane < k) {
-    const float w = num / den;
     a.plan.idx[t * k + lane] = my_e;
     a.plan.w[t * k + lane] = w;
     a.store_idx[t * k + lane] = my_e;
     a.store_w[t * k + lane] = w;
     s_idx[t * k + lane] = my_e;
   }
+}
+
+__device__ __forceinline__ OneTokenPlan one_token_plan_args(const RouterArgs& a) {
+  return OneTokenPlan{a.E, a.k, a.pmax, a.has_shared, a.big_min, a.store_idx, a.store_w, a.counters,
+                      a.record_bytes, (unsigned long long)a.E * a.H * 4ull};
 }
 
 // Phase 2 of the router, in one block: top-k per token from the logits lsrc [T][E]
@@ -178,59 +133,21 @@ __device__ __forceinline__ void router_finish(const RouterArgs& a, const float* 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int E = a.E, T = a.T, k = a.k, pmax = a.pmax;
   if (T == 1 && a.big_min != 1) {
-    // one token, in warp 0 alone: every selected expert has one pass, the passes in
-    // ascending expert id, the shared expert's last; no expert reaches a dense group
+    // one token, in warp 0 alone (route.cuh's one-token plan)
     if (warp != 0) return;
-    if (SMALL || E <= 128) topk_token<4>(a, lsrc, global_src, 0, lane, s_idx);
-    else if (E <= 256) topk_token<8>(a, lsrc, global_src, 0, lane, s_idx);
-    else if (E <= 512) topk_token<16>(a, lsrc, global_src, 0, lane, s_idx);
-    else topk_token<32>(a, lsrc, global_src, 0, lane, s_idx);
-    __syncwarp();
-    const int ee = lane < k ? s_idx[lane] : 0x7fffffff;
-    int p = 0;   // rank of the expert among the k by id (the k ids are distinct)
-    for (int j = 0; j < k; ++j) p += __shfl_sync(0xffffffffu, ee, j) < ee ? 1 : 0;
-    if (lane < k) {
-      a.plan.uniq[p] = ee;
-      a.plan.pass_expert[p] = ee;
-      a.plan.pass_ntok[p] = 1;
-      a.plan.pass_tok[p * pmax] = 0;
-      a.plan.pair_pass[lane] = p;
-      a.plan.pair_slot[lane] = 0;
-    }
-    const int n_pass = k + (a.has_shared ? 1 : 0);
-    if (a.big_min > 0)
-      for (int q = lane; q < n_pass; q += 32) a.plan.small_order[q] = q;
-    if (lane == 0) {
-      if (a.has_shared) {
-        a.plan.pass_tok[k * pmax] = 0;
-        a.plan.shared_pass[0] = k;
-        a.plan.shared_slot[0] = 0;
-        a.plan.pass_expert[k] = E;
-        a.plan.pass_ntok[k] = 1;
-      }
-      a.plan.hdr->n_pass = n_pass;
-      a.plan.hdr->n_routed_pass = k;
-      a.plan.hdr->n_uniq = k;
-      a.plan.hdr->T = 1;
-      a.plan.hdr->n_big = 0;
-      a.plan.hdr->n_small = n_pass;
-      DevCounters* dc = a.counters;
-      atomicAdd(&dc->forwards, 1ull);
-      atomicAdd(&dc->tokens, 1ull);
-      atomicAdd(&dc->lookups, (unsigned long long)k);
-      atomicAdd(&dc->bytes_touched, (unsigned long long)n_pass * a.record_bytes);
-      atomicAdd(&dc->bytes_router, (unsigned long long)E * a.H * 4ull);
-      *a.ticket = 0u;  // ready for the next launch (stream-ordered)
-    }
+    int my_e;
+    float my_l;
+    if (SMALL) warp_topk<4>(lsrc, global_src, E, k, lane, my_e, my_l);
+    else warp_topk_any(lsrc, global_src, E, k, lane, my_e, my_l);
+    const float w = route_weight(a.kind, k, lane, my_l);
+    write_one_token_plan(a.plan, one_token_plan_args(a), lane, my_e, w, one_token_pass(k, lane, my_e));
+    if (lane == 0) *a.ticket = 0u;  // ready for the next launch (stream-ordered)
     return;
   }
   // ---------------- phase 2a: top-k per token (one warp per token)
   for (int t = warp; t < T; t += nwarps) {
     const float* src = lsrc + (size_t)t * E;
-    if (SMALL || E <= 128) topk_token<4>(a, src, global_src, t, lane, s_idx);
-    else if (E <= 256) topk_token<8>(a, src, global_src, t, lane, s_idx);
-    else if (E <= 512) topk_token<16>(a, src, global_src, t, lane, s_idx);
-    else topk_token<32>(a, src, global_src, t, lane, s_idx);
+    topk_token<SMALL>(a, src, global_src, t, lane, s_idx);
   }
   __syncthreads();
 
@@ -483,6 +400,7 @@ __global__ void __launch_bounds__(256, MINB) router_kernel(RouterArgs a) {
     logits[(size_t)t * a.E + ee] = v;
   }
   if (threadIdx.x == 0) a.ticket[1 + g] = 0u;  // ready for the next launch (stream-ordered)
+  if (a.defer) return;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_flag = (atomicAdd(a.ticket, 1u) == (unsigned)NG - 1);
@@ -652,6 +570,7 @@ __global__ void __launch_bounds__(256, MINB) router_cluster_kernel(RouterArgs a)
       logits[(size_t)t * a.E + g * REPB + w] = v;
     }
   }
+  if (a.defer) return;
   // the group's ticket: its release publishes the logits (written before the barrier),
   // and the last group's acquire makes every group's logits visible to this block
   __syncthreads();
@@ -789,7 +708,9 @@ __global__ void __launch_bounds__(RSMALL_THREADS) router_small_kernel(RouterArgs
     float v = 0.f;
     for (int ss = 0; ss < NS; ++ss) v += spart[(size_t)q * NS + ss];
     slog[q] = v;
+    if (a.defer) a.partial[(size_t)NS * T * E + q] = v;   // where the other kernels keep the logits
   }
+  if (a.defer) return;
   __syncthreads();
   router_finish<true>(a, slog, false, s_cnt, s_off, s_idx, s_pos, &s_routed);
 }

@@ -25,18 +25,21 @@
 // 16 warps per block.
 #include "common.cuh"
 #include "kernels.h"
+#include "route.cuh"
 
 namespace moe {
 
 constexpr int RV_NW = 16;                              // warps per block (divides 96)
 constexpr int RV_LUT_BYTES = 3 * 256 * RVQ_KS * 4;     // 196608
 constexpr int RV_VIN_BYTES = RVQ_KS * RVQ_GROUP * 4;   // 2048
-constexpr int RV_SMEM = RV_LUT_BYTES + RV_VIN_BYTES;
+constexpr int RV_PE_BYTES = 33 * 4;                      // pass -> expert of a token routed here (k <= 32)
+constexpr int RV_SMEM = RV_LUT_BYTES + RV_VIN_BYTES + RV_PE_BYTES;
 constexpr int RV_HQ = RVQ_TASK_BYTES / 512 / 2;        // 6 uint4 per lane per half task (32 groups)
 
 // The table starts the block's dynamic shared memory.  Where that memory starts at
-// shared address RV_DYN_BASE (1024 on this part: the reserved 1 KB comes first) a lookup
-// is a single shared load [prmt result + constant]; elsewhere the base is added.
+// shared address RV_DYN_BASE (1024 on this part: the reserved 1 KB comes first, and the
+// kernel declares no static shared memory, which would come before it) a lookup is a
+// single shared load [prmt result + constant]; elsewhere the base is added.
 constexpr uint32_t RV_DYN_BASE = 1024;
 
 // Table entry at shared address addr + delta + OFF (delta = 0 on the fast path).  The
@@ -107,7 +110,9 @@ struct RvUnit {
 };
 
 template <bool DOWN>
-__device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, int p_begin, const RecGeom& rg) {
+// s_pe: pass -> expert when the kernel routed the token itself (one token), else null
+__device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, int p_begin, const RecGeom& rg,
+                                          const int* s_pe) {
   constexpr int mats = DOWN ? 1 : 2;
   RvUnit U;
   U.ks = u % nks;
@@ -115,8 +120,8 @@ __device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, i
   U.m = pm % mats;
   const int pi = pm / mats;
   U.pass = a.range.order ? __ldcg(a.range.order + p_begin + pi) : p_begin + pi;
-  U.expert = __ldcg(a.plan.pass_expert + U.pass);
-  U.tok = DOWN ? 0 : __ldcg(a.plan.pass_tok + U.pass);
+  U.expert = s_pe ? s_pe[U.pass] : __ldcg(a.plan.pass_expert + U.pass);
+  U.tok = (DOWN || s_pe) ? 0 : __ldcg(a.plan.pass_tok + U.pass);
   U.base = expert_record(a, U.expert) + (DOWN ? rg.off[2] : (U.m == 0 ? rg.off[0] : rg.off[1]));
   return U;
 }
@@ -128,21 +133,21 @@ __device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, i
 constexpr int RV_RND_COST = 8;
 constexpr int RV_SEG_COST = 7;
 
-// Split of u_n units over the grid: groups of g blocks, every full group holding kk whole
+// The split itself (BlockSplit): groups of g blocks, every full group holding kk whole
 // units and spending at most m_full per block; the G mod g blocks left over form the last
 // group, which holds the rest of the units at most m_rem per block.
-struct RvSplit {
-  int g, kk, m_full, m_rem;
-};
+
+__host__ __device__ __forceinline__ int imin_hd(int x, int y) { return x < y ? x : y; }
+__host__ __device__ __forceinline__ int imax_hd(int x, int y) { return x > y ? x : y; }
 
 // Greedy advance: from task u * n + r (r a multiple of RV_NW), take whole rounds of unit
 // u, then of the next units, while the budget B pays a segment and a round; stops at
 // unit u_end.  nr = rounds per unit.  Returns the budget spent.
-__device__ __forceinline__ int rv_advance(int& u, int& r, int B, int u_end, int nr) {
+__host__ __device__ __forceinline__ int rv_advance(int& u, int& r, int B, int u_end, int nr) {
   const int B0 = B;
   while (u < u_end && B >= RV_SEG_COST + RV_RND_COST) {
     const int left = nr - r / RV_NW;
-    const int take = min((B - RV_SEG_COST) / RV_RND_COST, left);
+    const int take = imin_hd((B - RV_SEG_COST) / RV_RND_COST, left);
     B -= RV_SEG_COST + RV_RND_COST * take;
     if (take == left) {
       ++u;
@@ -155,7 +160,7 @@ __device__ __forceinline__ int rv_advance(int& u, int& r, int B, int u_end, int 
 }
 
 // cost of the tasks from u * n + r to the end of unit u_end - 1
-__device__ __forceinline__ int rv_tail_cost(int u, int r, int u_end, int nr) {
+__host__ __device__ __forceinline__ int rv_tail_cost(int u, int r, int u_end, int nr) {
   if (u >= u_end) return 0;
   int c = 0;
   if (r > 0) {
@@ -167,42 +172,58 @@ __device__ __forceinline__ int rv_tail_cost(int u, int r, int u_end, int nr) {
 
 // `units` whole units over gg blocks: the budget per block (x) and the largest block cost
 // (y) of the greedy split, whose last block takes what is left
-__device__ __forceinline__ int2 rv_group(int units, int gg, int nr) {
+__host__ __device__ __forceinline__ int2 rv_group(int units, int gg, int nr) {
   const int W = RV_SEG_COST + RV_RND_COST * nr;
   const int M0 = (units * W + RV_SEG_COST * (gg - 1) + gg - 1) / gg;
   int u = 0, r = 0, mx = 0;
-  for (int i = 0; i < gg - 1; ++i) mx = max(mx, rv_advance(u, r, M0, units, nr));
-  return make_int2(M0, max(mx, rv_tail_cost(u, r, units, nr)));
+  for (int i = 0; i < gg - 1; ++i) mx = imax_hd(mx, rv_advance(u, r, M0, units, nr));
+  return make_int2(M0, imax_hd(mx, rv_tail_cost(u, r, units, nr)));
 }
 
-// The split of u_n units of n tasks over G blocks (G < u_n < 2 G) with the least largest
-// block cost among groups of g = 1..8 blocks and kk = ceil(u_n g / G) - 1 + {0, 1, 2}
-// units per full group: lane 3 (g - 1) + j of the warp evaluates one candidate, the warp
-// takes the cheapest (ties to the lower lane).  Every warp of every block computes the
-// same split.  g = 1, kk = ceil(u_n / G) is always valid.
-__device__ __forceinline__ RvSplit rv_plan(int u_n, int n, int G, int lane) {
+// Candidate c < 24 of the split of u_n units of n tasks over G blocks (G < u_n < 2 G):
+// groups of g = c / 3 + 1 blocks holding kk = ceil(u_n g / G) - 1 + c mod 3 units each.
+// Returns its largest block cost (RV_NO_SPLIT when it cannot hold the units) and the split.
+constexpr int RV_NO_SPLIT = (1 << 26) - 1;
+__host__ __device__ __forceinline__ int rv_candidate(int u_n, int n, int G, int c, BlockSplit& sp) {
   const int nr = (n + RV_NW - 1) / RV_NW;
-  int cost = (1 << 26) - 1;
-  RvSplit sp{1, 0, 0, 0};
-  if (lane < 24) {
-    const int g = lane / 3 + 1, ng = G / g, rem = G - ng * g;
-    const int kk = (u_n * g + G - 1) / G - 1 + lane % 3;
-    const int ur = max(0, u_n - ng * kk);
-    if (ng > 0 && kk >= 1 && (ur == 0 || rem > 0)) {
-      const int2 f = rv_group(min(kk, u_n), g, nr);
-      const int2 rr = ur > 0 ? rv_group(ur, rem, nr) : make_int2(0, 0);
-      cost = min(max(f.y, rr.y), (1 << 26) - 1);
-      sp = RvSplit{g, kk, f.x, rr.x};
-    }
-  }
+  const int g = c / 3 + 1, ng = G / g, rem = G - ng * g;
+  const int kk = (u_n * g + G - 1) / G - 1 + c % 3;
+  const int ur = imax_hd(0, u_n - ng * kk);
+  if (ng == 0 || kk < 1 || (ur > 0 && rem == 0)) return RV_NO_SPLIT;
+  const int2 f = rv_group(imin_hd(kk, u_n), g, nr);
+  const int2 rr = ur > 0 ? rv_group(ur, rem, nr) : make_int2(0, 0);
+  sp = BlockSplit{g, kk, f.x, rr.x};
+  return imin_hd(imax_hd(f.y, rr.y), RV_NO_SPLIT);
+}
+
+// The split with the least largest block cost among the 24 candidates (ties to the lower
+// candidate; g = 1, kk = ceil(u_n / G) always holds the units).  On the device lane c of a
+// warp evaluates candidate c and the warp takes the cheapest, so every warp of every block
+// computes the same split; the host version gives the same one.
+__device__ __forceinline__ BlockSplit rv_plan(int u_n, int n, int G, int lane) {
+  BlockSplit sp{1, 0, 0, 0};
+  const int cost = lane < 24 ? rv_candidate(u_n, n, G, lane, sp) : RV_NO_SPLIT;
   const unsigned best = __reduce_min_sync(0xffffffffu, (unsigned)cost << 5 | (unsigned)lane);
   const int wl = best & 31;
-  return RvSplit{__shfl_sync(0xffffffffu, sp.g, wl), __shfl_sync(0xffffffffu, sp.kk, wl),
-                 __shfl_sync(0xffffffffu, sp.m_full, wl), __shfl_sync(0xffffffffu, sp.m_rem, wl)};
+  return BlockSplit{__shfl_sync(0xffffffffu, sp.g, wl), __shfl_sync(0xffffffffu, sp.kk, wl),
+                    __shfl_sync(0xffffffffu, sp.m_full, wl), __shfl_sync(0xffffffffu, sp.m_rem, wl)};
+}
+static BlockSplit rv_plan_host(int u_n, int n, int G) {
+  BlockSplit best{1, 0, 0, 0};
+  int best_cost = RV_NO_SPLIT + 1;
+  for (int c = 0; c < 24; ++c) {
+    BlockSplit sp{};
+    const int cost = rv_candidate(u_n, n, G, c, sp);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = sp;
+    }
+  }
+  return best;
 }
 
 // block b's task range [t0, t1) under the split sp
-__device__ __forceinline__ void rv_range(const RvSplit& sp, int u_n, int n, int G, int b, int& t0, int& t1) {
+__device__ __forceinline__ void rv_range(const BlockSplit& sp, int u_n, int n, int G, int b, int& t0, int& t1) {
   const int nr = (n + RV_NW - 1) / RV_NW;
   const int ng = G / sp.g, j = b / sp.g, i = b - j * sp.g;
   int u0, u1, B, gj;
@@ -252,13 +273,12 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   // Work split.  Every unit (pass, matrix, k-slice) costs a table build, so with no more
   // units than blocks each unit goes to its own group of blocks, which split its tasks:
   // every block builds one table; with at least two units per block, blocks take whole
-  // units (contiguous unit ranges); in between, rv_plan balances the blocks' costs.  In
-  // gate/up a pass count fixed at launch (one token) gives that balanced split before the
-  // wait, while the kernel before still runs (down waits later anyway).
+  // units (contiguous unit ranges); in between, rv_plan balances the blocks' costs.  A
+  // pass count fixed at launch (one token) comes with that split made on the host.
   int t0 = 0, t1 = -1;   // t1 < 0: not split yet
-  if (!DOWN && a.range.p_end >= 0) {
+  if (a.split.g > 0) {
     const int u_n = max(0, a.range.p_end - p_begin) * mats * nks;
-    if (u_n > G && u_n < 2 * G) rv_range(rv_plan(u_n, ntask, G, lane), u_n, ntask, G, blockIdx.x, t0, t1);
+    rv_range(a.split, u_n, ntask, G, blockIdx.x, t0, t1);
   }
   if (!DOWN) {
     pdl_wait();
@@ -284,6 +304,26 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
       t1 = 0;
     }
   }
+  // One token routed here (the router deferred, writing the logits only): warp 0 takes
+  // the top-k (gate/up after its wait; down before it, since the logits are older than
+  // the gate/up kernel, which waited for them before letting this one start), gate/up's
+  // block 0 writes the plan for the kernels after, and each block keeps pass -> expert.
+  int* s_pe = reinterpret_cast<int*>(smem + RV_LUT_BYTES + RV_VIN_BYTES);
+  if (a.route_logits) {
+    if (warp == 0) {
+      const int k = a.route.k;
+      int my_e;
+      float my_l;
+      if (a.E <= 256) warp_topk<8>(a.route_logits, true, a.E, k, lane, my_e, my_l);
+      else warp_topk<16>(a.route_logits, true, a.E, k, lane, my_e, my_l);
+      const int pp = one_token_pass(k, lane, my_e);
+      if (lane < k) s_pe[pp] = my_e;
+      if (lane == 0) s_pe[k] = a.E;   // the shared expert's pass, when there is one
+      if (!DOWN && blockIdx.x == 0)
+        write_one_token_plan(a.plan, a.route, lane, my_e, route_weight(a.route_kind, k, lane, my_l), pp);
+    }
+    __syncthreads();
+  }
   const uint32_t l4 = (uint32_t)lane << 2;
   const uint32_t delta = smem_u32(smem) - RV_DYN_BASE;   // 0 on the fast path
 
@@ -295,7 +335,7 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   for (int i = t0; i < t1;) {
     const int u = i / ntask;
     const int seg_end = min(t1, (u + 1) * ntask);
-    const RvUnit U = rv_unit<DOWN>(a, u, nks, p_begin, rg);
+    const RvUnit U = rv_unit<DOWN>(a, u, nks, p_begin, rg, a.route_logits ? s_pe : nullptr);
     const uint8_t* codes = U.base + RVQ_CB_BYTES + (size_t)U.ks * ntask * RVQ_TASK_BYTES;
     const int useg = u * ntask;
 
@@ -477,10 +517,23 @@ cudaError_t rvq_set_attributes() {
   return cudaFuncSetAttribute(rvq_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, RV_SMEM);
 }
 
-cudaError_t launch_rvq_gateup(const ExpertArgs& a, int grid, cudaStream_t s) {
+// the host-made split of a pass count fixed at launch, when units are between one and two
+// per block (g = 0: none, the kernel splits)
+static BlockSplit host_split(const ExpertArgs& a, bool down, int grid) {
+  if (a.range.p_end < 0) return BlockSplit{0, 0, 0, 0};
+  const MatGeom g = rec_geom(WFMT_RVQ, a.H, a.F).m[down ? 2 : 0];
+  const int u_n = std::max(0, a.range.p_end - a.range.p_begin) * (down ? 1 : 2) * g.nks;
+  if (u_n <= grid || u_n >= 2 * grid) return BlockSplit{0, 0, 0, 0};
+  return rv_plan_host(u_n, g.ntask, grid);
+}
+cudaError_t launch_rvq_gateup(const ExpertArgs& a0, int grid, cudaStream_t s) {
+  ExpertArgs a = a0;
+  a.split = host_split(a0, false, grid);
   return launch_pdl(rvq_kernel<false>, grid, RV_NW * 32, RV_SMEM, s, a);
 }
-cudaError_t launch_rvq_down(const ExpertArgs& a, int grid, cudaStream_t s) {
+cudaError_t launch_rvq_down(const ExpertArgs& a0, int grid, cudaStream_t s) {
+  ExpertArgs a = a0;
+  a.split = host_split(a0, true, grid);
   return launch_pdl(rvq_kernel<true>, grid, RV_NW * 32, RV_SMEM, s, a);
 }
 

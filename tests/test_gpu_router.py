@@ -7,7 +7,8 @@ W[e] = c_e * u with u exact in a few bits and c_e a small integer level, so the 
 expert e is c_e * (u . x) and every level is a run of exact ties.  The cases cover few
 candidates at the selection threshold, between 32 and 64 of them, and more than 64 (every
 logit equal), and the three router kernels (one block, clusters of slices, more than 8
-slices).
+slices), with several tokens (the router's own top-k) and with one (the top-k taken in the
+RVQ expert kernels).
 """
 import numpy as np
 import pytest
@@ -40,6 +41,10 @@ def _expected(c, s, k):
     (1024, 40, 4, 0, 0, 2),      # every logit 0: 40 candidates, ids 0..3
     (7168, 384, 16, 0, 0, 1),    # every logit 0, 384 experts, clusters of 7 slices
     (8448, 72, 8, 6, 1, 2),      # 9 slices (no clusters), 12 per level
+    # one token: the router writes the logits only and the RVQ kernels take the top-k
+    (256, 32, 8, 4, 0, 1),       # one-block router
+    (1024, 256, 8, 2, 1, 1),     # clusters, more than 64 candidates
+    (8448, 72, 8, 6, 1, 1),      # 9 slices (no clusters)
 ])
 def test_exact_ties_take_the_lower_id(H, E, k, n_levels, router, T):
     import routed_expert_ffn_03_gb300 as M

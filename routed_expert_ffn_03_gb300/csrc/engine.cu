@@ -929,10 +929,13 @@ static moe_status forward_impl(moe_ctx* c, int layer, const void* x, float* xres
   ra.counters = c->d_counters;
   ra.record_bytes = c->rec_bytes;
   ra.big_min = c->big_min;
-  // One resident RVQ token: the router writes the logits only and the two RVQ kernels
-  // take the top-k themselves (one kernel boundary and the router's last-block step fewer
-  // on the way to the first expert lookup).
-  ra.defer = (!c->streamed && c->cfg.wfmt == MOE_W_RVQ3_G8 && T == 1 && c->big_min == 0 && k <= 32 && E <= 512) ? 1 : 0;
+  // One resident RVQ token with a router of many blocks: the router writes the logits
+  // only and the two RVQ kernels take the top-k themselves (the router's last-block step
+  // and a dependent plan read fewer on the way to the first expert lookup).  A one-block
+  // router leaves the other SMs free, so the expert kernel starts early anyway and
+  // routing in it would only add to its path.
+  ra.defer = (!c->streamed && c->cfg.wfmt == MOE_W_RVQ3_G8 && T == 1 && c->big_min == 0 && k <= 32 && E <= 512 &&
+              !router_one_block(H, T, E)) ? 1 : 0;
   if (c->prof && !c->streamed) CK(cudaEventRecordWithFlags(c->prof_ev[(size_t)layer * 5], s, cudaEventRecordExternal));
   CK(launch_router(ra, c->num_sms, s));
   ++c->launches;

@@ -40,6 +40,7 @@ struct RouterArgs {
   int defer;             // one token: write the logits only, the expert kernels route (see ExpertArgs)
 };
 cudaError_t launch_router(const RouterArgs& a, int num_sms, cudaStream_t s);
+bool router_one_block(int H, int T, int E);   // the router runs as a single block
 cudaError_t router_set_attributes();
 int router_nch(int H);
 int router_tickets(int E);

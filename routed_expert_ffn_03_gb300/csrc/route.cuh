@@ -149,4 +149,21 @@ __device__ __forceinline__ void write_one_token_plan(const PlanPtrs& plan, const
   }
 }
 
+// Routing of one token inside an expert kernel (the router deferred, ExpertArgs
+// route_logits set), by warp 0 of a block: the top-k of the logits (E <= 512), each pass's
+// expert into s_pe (pass p = the p-th selected expert by id, the shared expert's pass k
+// last), and with write_plan the plan for the kernels after (one block of the first
+// expert kernel).
+__device__ __forceinline__ void route_one_token(const ExpertArgs& a, int lane, int* s_pe, bool write_plan) {
+  const int k = a.route.k;
+  int my_e;
+  float my_l;
+  if (a.E <= 256) warp_topk<8>(a.route_logits, true, a.E, k, lane, my_e, my_l);
+  else warp_topk<16>(a.route_logits, true, a.E, k, lane, my_e, my_l);
+  const int pp = one_token_pass(k, lane, my_e);
+  if (lane < k) s_pe[pp] = my_e;
+  if (lane == 0) s_pe[k] = a.E;
+  if (write_plan) write_one_token_plan(a.plan, a.route, lane, my_e, route_weight(a.route_kind, k, lane, my_l), pp);
+}
+
 }  // namespace moe

@@ -606,6 +606,8 @@ constexpr int ROUTER_SMEM_MAX = 160 * 1024;
 __host__ __device__ __forceinline__ bool router_small_fits(int H, int T, int E) {
   return E * cdiv(H, RSW) <= RSMALL_THREADS / 32 && T * H <= 32768 && T <= 32;
 }
+bool router_one_block(int H, int T, int E) { return router_small_fits(H, T, E); }
+
 // bf16 inputs, slice partials, logits and phase 2's arrays
 size_t router_small_smem(int H, int T, int E, int k) {
   return ((size_t)T * H / 2 + (size_t)T * E * cdiv(H, RSW) + (size_t)T * E + (size_t)2 * E + (size_t)2 * T * k) * 4;

@@ -310,18 +310,7 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   // block 0 writes the plan for the kernels after, and each block keeps pass -> expert.
   int* s_pe = reinterpret_cast<int*>(smem + RV_LUT_BYTES + RV_VIN_BYTES);
   if (a.route_logits) {
-    if (warp == 0) {
-      const int k = a.route.k;
-      int my_e;
-      float my_l;
-      if (a.E <= 256) warp_topk<8>(a.route_logits, true, a.E, k, lane, my_e, my_l);
-      else warp_topk<16>(a.route_logits, true, a.E, k, lane, my_e, my_l);
-      const int pp = one_token_pass(k, lane, my_e);
-      if (lane < k) s_pe[pp] = my_e;
-      if (lane == 0) s_pe[k] = a.E;   // the shared expert's pass, when there is one
-      if (!DOWN && blockIdx.x == 0)
-        write_one_token_plan(a.plan, a.route, lane, my_e, route_weight(a.route_kind, k, lane, my_l), pp);
-    }
+    if (warp == 0) route_one_token(a, lane, s_pe, !DOWN && blockIdx.x == 0);
     __syncthreads();
   }
   const uint32_t l4 = (uint32_t)lane << 2;

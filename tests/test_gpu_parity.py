@@ -49,11 +49,12 @@ def test_tiny_config_rvq_top2_softmax():
     (2048, 64, 40, 4, 5, 0, True),      # router clusters of 2 slices
     (2560, 128, 24, 3, 40, 1, False),   # clusters of 3 (a ragged slice), two 32-token staging groups
     (8448, 64, 40, 4, 3, 1, False),     # 9 slices: the router without clusters
-    # one token: the router writes the logits only, the RVQ kernels route (every router kernel)
+    # one token: the router writes the logits only, the RVQ kernels route (both many-block
+    # router kernels)
     (2048, 64, 40, 4, 1, 0, True),      # clusters of 2 slices, shared expert
     (8448, 64, 40, 4, 1, 1, False),     # 9 slices
     (128, 64, 300, 8, 1, 1, True),      # E > 256, sigmoid + shared
-    (264, 200, 33, 3, 1, 0, True),      # ragged k-slice, one-block router
+    (264, 200, 33, 3, 1, 0, True),      # ragged k-slice, clusters of one slice
 ])
 def test_rvq_odd_shapes(H, F, E, k, T, router, shared):
     _run(LayerSpec(H, F, E, k, S.RVQ, router=router, shared=shared, seed=H + F + E), T)

@@ -8,7 +8,7 @@ expert e is c_e * (u . x) and every level is a run of exact ties.  The cases cov
 candidates at the selection threshold, between 32 and 64 of them, and more than 64 (every
 logit equal), and the three router kernels (one block, clusters of slices, more than 8
 slices), with several tokens (the router's own top-k) and with one (the top-k taken in the
-RVQ expert kernels).
+RVQ expert kernels, except behind the one-block router).
 """
 import numpy as np
 import pytest
@@ -41,7 +41,8 @@ def _expected(c, s, k):
     (1024, 40, 4, 0, 0, 2),      # every logit 0: 40 candidates, ids 0..3
     (7168, 384, 16, 0, 0, 1),    # every logit 0, 384 experts, clusters of 7 slices
     (8448, 72, 8, 6, 1, 2),      # 9 slices (no clusters), 12 per level
-    # one token: the router writes the logits only and the RVQ kernels take the top-k
+    # one token: a router of many blocks writes the logits only and the RVQ kernels take
+    # the top-k; the one-block router still routes by itself
     (256, 32, 8, 4, 0, 1),       # one-block router
     (1024, 256, 8, 2, 1, 1),     # clusters, more than 64 candidates
     (8448, 72, 8, 6, 1, 1),      # 9 slices (no clusters)

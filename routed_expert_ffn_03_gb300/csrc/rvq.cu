@@ -126,10 +126,12 @@ __device__ __forceinline__ RvUnit rv_unit(const ExpertArgs& a, int u, int nks, i
   return U;
 }
 
-// Block split cost model, fitted to per-warp timestamps of the gate/up kernel: a warp's
-// task takes ~2.3 us and warps take the tasks of a unit in rounds of RV_NW, so a block
-// pays one round (RV_RND_COST) per started round of each unit it touches, plus ~2.0 us
-// (RV_SEG_COST) per unit for the table build and the unit's start.
+// Block split cost model, fitted to per-warp timestamps of the gate/up kernel: warps take
+// the tasks of a unit in rounds of RV_NW (one task each, ~2.3 us with some blocks idle,
+// ~2.9 us with every block streaming), so a block pays one round (RV_RND_COST) per
+// started round of each unit it touches, plus a table build and the unit's start per unit
+// (RV_SEG_COST, ~2.0 to ~2.9 us).  Costs 6 to 9 per 8 of a round give the same split on
+// the layer shapes measured.
 constexpr int RV_RND_COST = 8;
 constexpr int RV_SEG_COST = 7;
 

@@ -256,6 +256,16 @@ moe_status moe_route_noalloc(const uint16_t* x_bf16, const float* W, int T, int 
 moe_status moe_profile(moe_ctx* ctx, int enable);
 moe_status moe_profile_read(moe_ctx* ctx, double* ms, int* n_layers);
 
+/* Work split of the RVQ lookup kernel (host code, no device): for u_n units of ntask
+ * 32-row tasks over `grid` blocks with grid < u_n < 2 grid (a unit = one pass, matrix and
+ * 512-input k-slice, each costing a table build), writes block b's task range
+ * [t0[b], t1[b]) for b < grid, the same ranges the kernel's blocks take: groups of blocks
+ * holding whole units, split greedily at rounds of 16 tasks, chosen for the least largest
+ * block cost.  Returns 0, or 1 (nothing written) when u_n is outside (grid, 2 grid),
+ * ntask or grid is not positive, u_n * ntask overflows an int or an array is null.  The
+ * caller owns t0 and t1 (grid ints each). */
+int moe_rvq_block_split(int u_n, int ntask, int grid, int* t0, int* t1);
+
 /* ---- test hooks (no counterpart in the pages; failure injection on the host) ---- */
 
 /* Make the next `n` host-to-device miss copies fail as if cudaMemcpyAsync had

@@ -63,8 +63,9 @@ struct OneTokenPlan {
 };
 
 // Work split of the RVQ lookup kernel for a pass count fixed at launch, made on the host
-// (g = 0: none; the kernel splits).  Groups of g blocks, full groups holding kk units at
-// most m_full per block, the left-over blocks the rest at most m_rem per block.
+// (g = 0: none, the kernel splits; g = -1: equal task ranges).  Groups of g blocks, full
+// groups holding kk units at most m_full per block, the left-over blocks the rest at most
+// m_rem per block.
 struct BlockSplit {
   int g, kk, m_full, m_rem;
 };

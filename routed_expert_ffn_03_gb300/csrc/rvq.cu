@@ -210,32 +210,24 @@ __device__ __forceinline__ BlockSplit rv_plan(int u_n, int n, int G, int lane) {
   return BlockSplit{__shfl_sync(0xffffffffu, sp.g, wl), __shfl_sync(0xffffffffu, sp.kk, wl),
                     __shfl_sync(0xffffffffu, sp.m_full, wl), __shfl_sync(0xffffffffu, sp.m_rem, wl)};
 }
-static BlockSplit rv_plan_host(int u_n, int n, int G) {
-  BlockSplit best{1, 0, 0, 0};
-  int best_cost = RV_NO_SPLIT + 1;
-  for (int c = 0; c < 24; ++c) {
-    BlockSplit sp{};
-    const int cost = rv_candidate(u_n, n, G, c, sp);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = sp;
-    }
-  }
-  return best;
-}
-
 // block b's task range [t0, t1) under the split sp
-__device__ __forceinline__ void rv_range(const BlockSplit& sp, int u_n, int n, int G, int b, int& t0, int& t1) {
+__host__ __device__ __forceinline__ void rv_range(const BlockSplit& sp, int u_n, int n, int G, int b, int& t0,
+                                                  int& t1) {
+  if (sp.g < 0) {   // equal task ranges
+    t0 = (int)((long long)u_n * n * b / G);
+    t1 = (int)((long long)u_n * n * (b + 1) / G);
+    return;
+  }
   const int nr = (n + RV_NW - 1) / RV_NW;
   const int ng = G / sp.g, j = b / sp.g, i = b - j * sp.g;
   int u0, u1, B, gj;
   if (j < ng) {
-    u0 = min(u_n, j * sp.kk);
-    u1 = min(u_n, u0 + sp.kk);
+    u0 = imin_hd(u_n, j * sp.kk);
+    u1 = imin_hd(u_n, u0 + sp.kk);
     B = sp.m_full;
     gj = sp.g;
   } else {
-    u0 = min(u_n, ng * sp.kk);
+    u0 = imin_hd(u_n, ng * sp.kk);
     u1 = u_n;
     B = sp.m_rem;
     gj = G - ng * sp.g;
@@ -249,6 +241,33 @@ __device__ __forceinline__ void rv_range(const BlockSplit& sp, int u_n, int n, i
     rv_advance(u, r, B, u1, nr);
     t1 = u * n + r;
   }
+}
+
+// The host also weighs equal task ranges (g = -1), which a few unit counts favour; the
+// device leaves them out (their exact cost needs every block's range).
+static BlockSplit rv_plan_host(int u_n, int n, int G) {
+  BlockSplit best{1, 0, 0, 0};
+  int best_cost = RV_NO_SPLIT + 1;
+  for (int c = 0; c < 24; ++c) {
+    BlockSplit sp{};
+    const int cost = rv_candidate(u_n, n, G, c, sp);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = sp;
+    }
+  }
+  int eq_cost = 0;
+  for (int b = 0; b < G; ++b) {
+    int t0, t1, c = 0;
+    rv_range(BlockSplit{-1, 0, 0, 0}, u_n, n, G, b, t0, t1);
+    for (int i = t0; i < t1;) {   // segments: a table build and the started rounds of each unit
+      const int e = imin_hd(t1, (i / n + 1) * n);
+      c += RV_SEG_COST + RV_RND_COST * ((e - i + RV_NW - 1) / RV_NW);
+      i = e;
+    }
+    eq_cost = imax_hd(eq_cost, c);
+  }
+  return eq_cost < best_cost ? BlockSplit{-1, 0, 0, 0} : best;
 }
 
 template <bool DOWN>
@@ -278,7 +297,7 @@ __global__ void __launch_bounds__(RV_NW * 32, 1) rvq_kernel(ExpertArgs a) {
   // units (contiguous unit ranges); in between, rv_plan balances the blocks' costs.  A
   // pass count fixed at launch (one token) comes with that split made on the host.
   int t0 = 0, t1 = -1;   // t1 < 0: not split yet
-  if (a.split.g > 0) {
+  if (a.split.g != 0) {
     const int u_n = max(0, a.range.p_end - p_begin) * mats * nks;
     rv_range(a.split, u_n, ntask, G, blockIdx.x, t0, t1);
   }
@@ -517,6 +536,22 @@ static BlockSplit host_split(const ExpertArgs& a, bool down, int grid) {
   if (u_n <= grid || u_n >= 2 * grid) return BlockSplit{0, 0, 0, 0};
   return rv_plan_host(u_n, g.ntask, grid);
 }
+}  // namespace moe
+
+// Diagnostic (include/moe.h): the task ranges of the lookup kernel's blocks for u_n units
+// of ntask tasks over a grid of `grid` blocks when units are between one and two per
+// block, made by the same functions as the kernel's split.
+extern "C" int moe_rvq_block_split(int u_n, int ntask, int grid, int* t0, int* t1) {
+  if (u_n <= grid || u_n >= 2 * grid || ntask <= 0 || grid <= 0 || !t0 || !t1 ||
+      (long long)u_n * ntask > 0x7fffffffLL)
+    return 1;
+  const moe::BlockSplit sp = moe::rv_plan_host(u_n, ntask, grid);
+  for (int b = 0; b < grid; ++b) moe::rv_range(sp, u_n, ntask, grid, b, t0[b], t1[b]);
+  return 0;
+}
+
+namespace moe {
+
 cudaError_t launch_rvq_gateup(const ExpertArgs& a0, int grid, cudaStream_t s) {
   ExpertArgs a = a0;
   a.split = host_split(a0, false, grid);

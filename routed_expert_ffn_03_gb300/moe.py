@@ -93,6 +93,8 @@ def lib():
     L.moe_filetier_info.argtypes = [vp, ctypes.POINTER(FileTierStats)]
     L.moe_filetier_destroy.argtypes = [vp]
     L.moe_filetier_destroy.restype = None
+    L.moe_rvq_block_split.argtypes = [i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.moe_rvq_block_split.restype = ctypes.c_int
     for name in ("moe_create", "moe_register_router", "moe_register_expert", "moe_forward",
                  "moe_get_routing", "moe_residual_rmsnorm", "moe_stats", "moe_reset_stats",
                  "moe_destroy", "moe_debug_fail_copies", "moe_debug_wait_timeout",
@@ -130,6 +132,17 @@ def _stream(stream):
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def rvq_block_split(u_n: int, ntask: int, grid: int):
+    """The RVQ lookup kernel's task ranges (moe_rvq_block_split): lists t0, t1 of `grid`
+    blocks for u_n units of ntask tasks, grid < u_n < 2 grid.  Host code; raises ValueError
+    outside that range."""
+    t0 = (ctypes.c_int * grid)()
+    t1 = (ctypes.c_int * grid)()
+    if lib().moe_rvq_block_split(u_n, ntask, grid, t0, t1) != 0:
+        raise ValueError("moe_rvq_block_split(%d, %d, %d)" % (u_n, ntask, grid))
+    return list(t0), list(t1)
 
 
 def route_noalloc(x_bf16, W, T, H, E, k, router, idx, w, stream=None):

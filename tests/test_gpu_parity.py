@@ -55,6 +55,8 @@ def test_tiny_config_rvq_top2_softmax():
     (8448, 64, 40, 4, 1, 1, False),     # 9 slices
     (128, 64, 300, 8, 1, 1, True),      # E > 256, sigmoid + shared
     (264, 200, 33, 3, 1, 0, True),      # ragged k-slice, clusters of one slice
+    (256, 64, 64, 32, 1, 1, True),      # k = 32, the most the kernels route: 33 passes with the shared one
+    (256, 64, 600, 8, 1, 0, False),     # E > 512: the router routes by itself (32 keys per lane)
 ])
 def test_rvq_odd_shapes(H, F, E, k, T, router, shared):
     _run(LayerSpec(H, F, E, k, S.RVQ, router=router, shared=shared, seed=H + F + E), T)

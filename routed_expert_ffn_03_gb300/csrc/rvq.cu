@@ -201,7 +201,8 @@ __host__ __device__ __forceinline__ int rv_candidate(int u_n, int n, int G, int 
 // The split with the least largest block cost among the 24 candidates (ties to the lower
 // candidate; g = 1, kk = ceil(u_n / G) always holds the units).  On the device lane c of a
 // warp evaluates candidate c and the warp takes the cheapest, so every warp of every block
-// computes the same split; the host version gives the same one.
+// computes the same split; the host version (rv_plan_host) takes the same candidates in
+// the same order and also weighs equal task ranges.
 __device__ __forceinline__ BlockSplit rv_plan(int u_n, int n, int G, int lane) {
   BlockSplit sp{1, 0, 0, 0};
   const int cost = lane < 24 ? rv_candidate(u_n, n, G, lane, sp) : RV_NO_SPLIT;
@@ -210,6 +211,7 @@ __device__ __forceinline__ BlockSplit rv_plan(int u_n, int n, int G, int lane) {
   return BlockSplit{__shfl_sync(0xffffffffu, sp.g, wl), __shfl_sync(0xffffffffu, sp.kk, wl),
                     __shfl_sync(0xffffffffu, sp.m_full, wl), __shfl_sync(0xffffffffu, sp.m_rem, wl)};
 }
+
 // block b's task range [t0, t1) under the split sp
 __host__ __device__ __forceinline__ void rv_range(const BlockSplit& sp, int u_n, int n, int G, int b, int& t0,
                                                   int& t1) {
